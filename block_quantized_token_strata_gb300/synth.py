@@ -1,0 +1,134 @@
+"""Seeded synthetic inputs for the verify-window path and the prompt-chunk MoE.
+
+This module only draws random numbers (numpy PCG64) and lays them out in the byte formats that
+``include/strata.h`` documents. It holds none of the method's arithmetic: no quantisation of
+activations, no dot products, no scaling. Both the CUDA path and the CPU oracle take its outputs
+as plain inputs.
+
+Distributions (the workload recipe):
+  * weight block scales d = fp16(|N(0,1)| * 0.01), rounded to nearest-even by numpy;
+  * Q4 codes q ~ U{0..15} (two independent codes per byte, i.e. a uniform byte);
+  * Q8 codes q ~ U{-127..127};
+  * activations x ~ N(0,1) fp32, optionally with a Bernoulli(0.01) mask of elements scaled x20;
+  * MoE routing: k distinct experts per token drawn without replacement from a Zipf(1.1)
+    law over expert ranks, p_e proportional to (e+1)^-1.1, draw order = slot order.
+"""
+from __future__ import annotations
+
+import hashlib
+
+import numpy as np
+
+QK = 32
+Q4, Q8 = 0, 1
+_QBYTES = {Q4: 16, Q8: 32}
+
+
+def _rng(*key) -> np.random.Generator:
+    """A PCG64 stream keyed by any tuple of ints/strings (stable across machines)."""
+    words = []
+    for k in key:
+        if isinstance(k, str):
+            words.append(int.from_bytes(hashlib.sha256(k.encode()).digest()[:4], "little"))
+        else:
+            words.append(int(k) & 0xFFFFFFFF)
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(words)))
+
+
+def weight_nbytes(rows: int, cols: int, fmt: int) -> int:
+    nb = rows * (cols // QK)
+    return nb * (_QBYTES[fmt] + 2)
+
+
+class Weights:
+    """One block-quantized matrix: ``buf`` is the planar byte buffer of the C ABI.
+
+    ``codes(r0, r1)`` returns the integer codes of rows [r0, r1) as int16 [rows][cols] (Q4: 0..15,
+    Q8: -127..127) and ``scales`` the fp16 scales [rows][nb]; both are views of the same bytes,
+    decoded from the documented layout for tests that need them.
+    """
+
+    def __init__(self, rows: int, cols: int, fmt: int, buf: np.ndarray):
+        self.rows, self.cols, self.fmt, self.buf = rows, cols, fmt, buf
+        self.nb = cols // QK
+        self.plane_bytes = rows * self.nb * _QBYTES[fmt]
+
+    @property
+    def scales(self) -> np.ndarray:
+        return self.buf[self.plane_bytes:].view(np.float16).reshape(self.rows, self.nb)
+
+    def codes(self, r0: int = 0, r1: int | None = None) -> np.ndarray:
+        r1 = self.rows if r1 is None else r1
+        qb = _QBYTES[self.fmt]
+        plane = self.buf[r0 * self.nb * qb: r1 * self.nb * qb]
+        if self.fmt == Q8:
+            return plane.view(np.int8).astype(np.int16).reshape(r1 - r0, self.cols)
+        by = plane.reshape(r1 - r0, self.nb, 16)
+        out = np.empty((r1 - r0, self.nb, 32), dtype=np.int16)
+        out[:, :, :16] = by & 0x0F
+        out[:, :, 16:] = by >> 4
+        return out.reshape(r1 - r0, self.cols)
+
+
+def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
+    """A seeded [rows][cols] matrix in Q4 or Q8 (planar layout, see include/strata.h)."""
+    if cols % QK or rows <= 0:
+        raise ValueError("cols must be a multiple of 32 and rows positive")
+    rng = _rng("weights", rows, cols, fmt, *key)
+    nb = rows * (cols // QK)
+    d = (np.abs(rng.standard_normal(nb)) * 0.01).astype(np.float16)
+    if fmt == Q4:
+        plane = rng.integers(0, 256, size=nb * 16, dtype=np.uint8)
+    elif fmt == Q8:
+        plane = rng.integers(-127, 128, size=nb * 32, dtype=np.int8).view(np.uint8)
+    else:
+        raise ValueError("fmt")
+    buf = np.empty(plane.size + 2 * nb, dtype=np.uint8)
+    buf[:plane.size] = plane
+    buf[plane.size:] = d.view(np.uint8)
+    return Weights(rows, cols, fmt, buf)
+
+
+def make_activations(n: int, cols: int, *key, outliers: bool = False) -> np.ndarray:
+    """fp32 [n][cols] ~ N(0,1); with ``outliers`` 1% of the elements are scaled by 20."""
+    rng = _rng("act", n, cols, int(outliers), *key)
+    x = rng.standard_normal((n, cols), dtype=np.float32)
+    if outliers:
+        mask = rng.random((n, cols)) < 0.01
+        x[mask] *= np.float32(20.0)
+    return x
+
+
+def make_routing(n_tok: int, n_expert: int, k: int, *key, zipf_s: float = 1.1) -> np.ndarray:
+    """int32 [n_tok][k]: k distinct experts per token, Zipf(s) over ranks (rank e -> id e)."""
+    rng = _rng("route", n_tok, n_expert, k, *key)
+    p = (np.arange(1, n_expert + 1, dtype=np.float64)) ** (-zipf_s)
+    p /= p.sum()
+    ids = np.empty((n_tok, k), dtype=np.int32)
+    for t in range(n_tok):
+        ids[t] = rng.choice(n_expert, size=k, replace=False, p=p)
+    return ids
+
+
+# ---- named workloads ------------------------------------------------------------------------
+
+# Full verify window: 48 layers x (qkv 2048->5120, o 4096->2048, FFN up 2048->6144, down 6144->2048)
+# Q4, then a Q8 head 151936 x 2048. Each projection gets its own seeded input (layers not chained).
+WINDOW_LAYERS = 48
+WINDOW_HIDDEN = 2048
+WINDOW_PROJ = (("qkv", 5120, 2048), ("o", 2048, 4096), ("up", 6144, 2048), ("down", 2048, 6144))
+HEAD_VOCAB = 151936
+
+
+def window_shapes(layers: int = WINDOW_LAYERS):
+    """[(name, rows, cols, fmt)] of every matrix of the verify window, in launch order."""
+    out = []
+    for layer in range(layers):
+        for name, rows, cols in WINDOW_PROJ:
+            out.append((f"L{layer}.{name}", rows, cols, Q4))
+    out.append(("head", HEAD_VOCAB, WINDOW_HIDDEN, Q8))
+    return out
+
+
+# Prompt-chunk MoE: 128 experts, hidden 2048, inter 768, 3,256 tokens, top-8 Zipf(1.1)
+MOE_EXPERTS, MOE_HIDDEN, MOE_INTER, MOE_TOKENS, MOE_TOPK = 128, 2048, 768, 3256, 8

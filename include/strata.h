@@ -1,0 +1,188 @@
+/*
+ * strata.h — C ABI of the block-quantized multi-token verify path for one GB300 (sm_103a).
+ *
+ * What it computes. A speculative VERIFY window runs T tokens (the last accepted token plus T-1
+ * drafts) through dense block-quantized projections that are read from HBM once for all T tokens,
+ * and every token's output column is bit for bit what the single-token launch (T = 1) produces
+ * ("exact mode", multi-column MMVQ). The window ends in a vocabulary head whose per-token argmax
+ * picks the next id, ties going to the lower id. A grouped MoE-expert variant of the same block
+ * arithmetic covers prompt chunks.
+ *   Sources: Strata commit "wire multi-token kernels into Verifier and MtpDrafter CUDA graphs",
+ *   include/strata/core/verify.hpp, header comment (exact mode; one weight read for T tokens;
+ *   `xq_` = "T columns of q8_1"; the pool's output layout (n_tok*k, n_embd));
+ *   Strata pull request "sm_80 (GA100) tuning", commit message on the hoisted-load MMVQ-IL kernels
+ *   (exact integer forms, fixed accumulation order and xor tree);
+ *   dsv41-offload worker/tp2.py, module docstring "Collectives per draft step" and EmuComm.argmax
+ *   (argmax ties go to the lower id).
+ *
+ * Conventions for every call.
+ *   - All pointers except `const strata_expert*` host-side struct fields are DEVICE pointers unless
+ *     stated. The library allocates and frees nothing; the caller owns every buffer.
+ *   - Every call validates its arguments on the host first and returns a status code without
+ *     launching anything when they are wrong. Otherwise it enqueues kernels on `stream` and
+ *     returns at once (asynchronous); STRATA_ERR_CUDA reports a launch failure.
+ *   - Kernels are launched with programmatic dependent launch. Activations, outputs and workspace
+ *     are touched only after the preceding kernel on the stream has completed; WEIGHTS may be read
+ *     (prefetched into L2) while the preceding kernel is still running, so weight buffers must be
+ *     fully written before the kernel launched just ahead of the call on the same stream begins
+ *     (weights are static model data; a cudaMemcpy on the stream is a full dependency and is fine).
+ *   - Floating point is IEEE fp32 with round-to-nearest; no fast-math.
+ *
+ * Block formats (32 weights per block along a row; cols % 32 == 0; nb = cols / 32).
+ *   A weight matrix W[rows][cols] is ONE buffer holding two planes, the quant plane first:
+ *     STRATA_Q4: quant plane rows*nb*16 bytes; block (r, b) at byte offset (r*nb + b)*16;
+ *                byte j (0..15) holds element j in its low nibble and element j+16 in its high
+ *                nibble, each an unsigned code q in 0..15; the weight is w = d * (q - 8).
+ *     STRATA_Q8: quant plane rows*nb*32 bytes; block (r, b) at (r*nb + b)*32; byte j is element j
+ *                as a signed code q in -127..127; the weight is w = d * q.
+ *   followed by the scale plane: rows*nb IEEE binary16 scales d, little-endian, block (r, b) at
+ *   index r*nb + b. Total bytes = rows*nb*18 (Q4) or rows*nb*34 (Q8), the same as interleaved
+ *   {half d; codes} blocks, but both planes start on 16-byte boundaries so that every block's
+ *   codes are one or two aligned 16-byte loads. W must be 16-byte aligned.
+ *
+ * Quantized activations (q8_1-style, one scale and one sum per 32 values), for n rows of `cols`:
+ *     xq int8  [n][cols]   codes q in -127..127
+ *     xd fp32  [n][cols/32] scale d
+ *     xs int32 [n][cols/32] exact block sum  s = sum of the 32 codes
+ *   For each 32-block of x: amax = max|x_j| ; d = amax / 127 ; id = (d != 0) ? 1/d : 0 ;
+ *   q_j = roundf(x_j * id) (round half away from zero) ; s = sum q_j. Each operation is one IEEE
+ *   fp32 operation, so the codes are reproducible bit for bit on any IEEE machine.
+ *
+ * Block arithmetic shared by the GEMV family (one token t, one output row r):
+ *     isum[t][r][b] = sum_j wq_j * xq[t][32b+j]   with wq_j = q_j - 8 (Q4) or q_j (Q8), exact int32
+ *     y[t][r]       = sum_b (d_w[r][b] * xd[t][b]) * isum[t][r][b]      in fp32
+ *   The fp32 summation order is fixed by (rows, cols, fmt) only, never by T, so column t of a
+ *   T-token launch is bitwise equal to the T = 1 launch on that column's activations.
+ */
+#ifndef STRATA_H
+#define STRATA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (every entry point returns one of these) ---- */
+#define STRATA_OK              0   /* enqueued */
+#define STRATA_ERR_NULL       -1   /* a required pointer is NULL */
+#define STRATA_ERR_SHAPE      -2   /* cols % 32 != 0, a size <= 0 or above a stated maximum */
+#define STRATA_ERR_T          -3   /* T outside [1, STRATA_MAX_T] */
+#define STRATA_ERR_FMT        -4   /* unknown or unsupported block format */
+#define STRATA_ERR_CUDA       -5   /* a CUDA launch or attribute call failed */
+#define STRATA_ERR_EXPERT     -6   /* (device-side) an expert id was outside [0, n_expert) */
+#define STRATA_ERR_ALIGN      -7   /* a pointer is not aligned as the call requires */
+#define STRATA_ERR_WORKSPACE  -8   /* workspace NULL or smaller than the *_workspace() size */
+
+#define STRATA_MAX_T 8             /* verify windows hold 1..8 tokens */
+
+typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1 } strata_fmt;
+
+/* Static text for a status code (never NULL). */
+const char* strata_error_string(int status);
+
+/* Bytes of one weight matrix in `fmt` (0 if the shape is invalid). Host-only helper. */
+size_t strata_weight_bytes(int64_t rows, int64_t cols, int fmt);
+
+/*
+ * strata_quantize_act — fp32 activations to int8 blocks of 32 with an fp32 scale and block sum.
+ *   Source: verify.hpp header comment, member `xq_` ("T columns of q8_1") of the Strata commit
+ *   "wire multi-token kernels into Verifier and MtpDrafter CUDA graphs"; the scale is fp32.
+ *   x  : fp32 [n_rows][cols], row-major, 16-byte aligned.
+ *   xq : int8 [n_rows][cols], 16-byte aligned.   xd : fp32 [n_rows][cols/32].
+ *   xs : int32 [n_rows][cols/32].
+ *   n_rows >= 1 (any count: T tokens, or a prompt chunk's tokens); cols % 32 == 0, cols >= 32.
+ *   x must be finite. Errors: NULL, SHAPE, ALIGN, CUDA.
+ */
+int strata_quantize_act(const float* x, int64_t n_rows, int64_t cols,
+                        int8_t* xq, float* xd, int32_t* xs, cudaStream_t stream);
+
+/*
+ * strata_mmvq_multi — y[t][r] for T <= 8 tokens, reading W once.
+ *   Source: verify.hpp header comment (multi-column MMVQ in exact mode; dense weights read once
+ *   for T tokens), and the pull request "sm_80 (GA100) tuning", commit message on the hoisted
+ *   MMVQ-IL loads (integer dots exact, accumulation order and xor tree fixed).
+ *   W  : weight matrix [rows][cols] in `fmt` (layout above), 16-byte aligned.
+ *   xq, xd, xs : quantized activations of T rows of `cols` (xq 16-byte aligned).
+ *   y  : fp32 [T][rows] (token-major, rows contiguous), 4-byte aligned.
+ *   1 <= T <= 8, rows >= 1, cols % 32 == 0, 32 <= cols <= 65536.
+ *   Column t is bitwise identical for every T (see the block arithmetic above).
+ *   Errors: NULL, SHAPE, T, FMT, ALIGN, CUDA.
+ */
+int strata_mmvq_multi(const void* W, int64_t rows, int64_t cols, int fmt,
+                      const int8_t* xq, const float* xd, const int32_t* xs, int T,
+                      float* y, cudaStream_t stream);
+
+/*
+ * strata_head_argmax — vocabulary head GEMV fused with the per-token argmax.
+ *   Source: verify.hpp, Verifier::run (argmax after each token) and `h_out_/m_out_`, `copy_logits`;
+ *   tie rule from dsv41-offload worker/tp2.py, EmuComm.argmax and markov_local_argmax
+ *   ("ties -> lowest"): among equal maximal logits the lowest vocabulary id wins.
+ *   W : [vocab][cols] in `fmt` (Q8 in the verify configuration; Q4 is accepted too).
+ *   ids : int32 [T] device output.  logits : fp32 [T][vocab] or NULL (then not written).
+ *   workspace : device scratch of strata_head_argmax_workspace(vocab, T) bytes, 16-byte aligned;
+ *   its contents need no initialisation and are dead after the call.
+ *   Logits are computed exactly as strata_mmvq_multi computes y for the same W and activations.
+ *   Errors: NULL, SHAPE, T, FMT, ALIGN, WORKSPACE, CUDA.
+ */
+size_t strata_head_argmax_workspace(int64_t vocab, int T);
+int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt,
+                       const int8_t* xq, const float* xd, const int32_t* xs, int T,
+                       int32_t* ids, float* logits, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/*
+ * strata_moe_grouped — prompt-chunk MoE experts: per (token, slot) pair p = tok*k + slot routed to
+ * expert e = ids[p]:
+ *     g = W_gate[e] . xq(tok), u = W_up[e] . xq(tok)         (block arithmetic above, fp32)
+ *     h = silu(g) * u,  silu(g) = g / (1 + exp(-g))          (fp32)
+ *     (hq, hd, hs) = quantize_act(h)                          (same quantizer, blocks of 32)
+ *     y[p][:] = W_down[e] . hq                                (fp32, unweighted row per pair)
+ *   Source: verify.hpp, PoolMultiFn ("x_f (n_tok, n_embd), ids (n_tok, k) -> out (n_tok * k,
+ *   n_embd)"), and the pull request "sm_80 (GA100) tuning", commit messages on the fused prompt
+ *   MoE experts (one layer of 3,256 tokens; gate/up then down).
+ *   experts : DEVICE array of n_expert strata_expert; each field a device pointer to a Q4 matrix:
+ *             gate [inter][hidden], up [inter][hidden], down [hidden][inter].
+ *   ids : int32 [n_tok][k], device.   x : fp32 [n_tok][hidden], device, 16-byte aligned.
+ *   y   : fp32 [n_tok*k][hidden], device. Rows of pairs whose id is out of range are not written.
+ *   workspace : strata_moe_grouped_workspace(...) bytes, 256-byte aligned, contents need no
+ *               initialisation. err_word : device int32 or NULL; when non-NULL it is zeroed by the
+ *               call and then gets bit 0 set if any id was outside [0, n_expert).
+ *   hidden % 128 == 0, inter % 128 == 0, 1 <= k <= 16, n_expert >= 1.
+ *   Pairs are grouped per expert in ascending (token, slot) order; each row of y is written once.
+ *   Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA (STRATA_ERR_EXPERT is reported in err_word).
+ */
+typedef struct { const void* gate; const void* up; const void* down; } strata_expert;
+
+size_t strata_moe_grouped_workspace(int n_expert, int64_t n_tok, int k, int64_t hidden, int64_t inter);
+int strata_moe_grouped(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
+                       const int32_t* ids, int64_t n_tok, int k, const float* x, float* y,
+                       void* workspace, size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * strata_moe_debug_views — byte offsets, inside a strata_moe_grouped workspace, of the grouping
+ * and the re-quantized hidden activations a call leaves behind (test hook; no launch).
+ *   counts int32 [n_expert], offsets int32 [n_expert+1], pairs int32 [n_tok*k] (pair p = tok*k+slot,
+ *   grouped by expert, ascending within an expert), hq int8 [n_tok*k][inter] / hd fp32 /
+ *   hs int32 [n_tok*k][inter/32] indexed by position in `pairs`. Offsets are written to the seven
+ *   host size_t slots of `out` in that order. Errors: NULL, SHAPE.
+ */
+int strata_moe_debug_views(int n_expert, int64_t n_tok, int k, int64_t hidden, int64_t inter,
+                           size_t* out);
+
+/*
+ * strata_block_dots — test hook: the exact integer block dots the GEMV kernels accumulate,
+ *   isum[t][r][b] as int32 [T][rows][cols/32], computed by the same device block-dot code.
+ *   Source: the pull request "sm_80 (GA100) tuning", hoisted-load MMVQ-IL commit (exact integer
+ *   forms). Errors: NULL, SHAPE, T, FMT, ALIGN, CUDA.
+ */
+int strata_block_dots(const void* W, int64_t rows, int64_t cols, int fmt,
+                      const int8_t* xq, const int32_t* xs, int T, int32_t* isum,
+                      cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STRATA_H */

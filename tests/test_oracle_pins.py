@@ -1,0 +1,270 @@
+"""Pins of the CPU oracle against facts fixed outside it (no GPU).
+
+Every oracle function is checked against something other than itself:
+  * the fp16 decoder against numpy's binary16 conversion over all 65,536 patterns;
+  * the activation quantizer against hand-derived closed-form blocks (ties round away from zero,
+    a single outlier, all zeros) and the invariants its definition implies;
+  * the integer block dots against hand-computed one-block values and a brute-force numpy int64
+    matmul of codes this test packs itself;
+  * the fp64 GEMV against a brute-force dense fp64 matmul of the dequantized operands;
+  * the argmax tie rule against planted ties and numpy's first-occurrence argmax;
+  * the MoE grouping against numpy's stable sort, and the MoE rows against a dense brute force.
+Sources: Strata commit "wire multi-token kernels into Verifier and MtpDrafter CUDA graphs"
+(verify.hpp header comment: exact mode, q8_1 activations, pool layout (n_tok*k, n_embd));
+pull request "sm_80 (GA100) tuning" (exact integer block dots); dsv41-offload worker/tp2.py
+(argmax ties to the lowest id).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from block_quantized_token_strata_gb300 import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ---- this test's own packer of the documented planar layout ------------------------------------
+def pack_q4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """codes uint [rows][cols] in 0..15, scales float16 [rows][cols/32] -> planar bytes."""
+    rows, cols = codes.shape
+    nb = cols // 32
+    c = codes.reshape(rows, nb, 32).astype(np.uint8)
+    plane = (c[:, :, :16] | (c[:, :, 16:] << 4)).reshape(-1)
+    return np.concatenate([plane, np.asarray(scales, np.float16).reshape(-1).view(np.uint8)])
+
+
+def pack_q8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    plane = np.asarray(codes, np.int8).reshape(-1).view(np.uint8)
+    return np.concatenate([plane, np.asarray(scales, np.float16).reshape(-1).view(np.uint8)])
+
+
+# ---- fp16 decoder -------------------------------------------------------------------------------
+def test_half_decoder_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ---- activation quantizer -------------------------------------------------------------------------
+def test_quantize_zero_block(orc):
+    q, d, s = orc.quantize_act(np.zeros((2, 64), np.float32))
+    assert not q.any() and not d.any() and not s.any()
+
+
+def test_quantize_half_way_ties_round_away_from_zero(orc):
+    # amax = 127 gives d = 127/127 = 1 and 1/d = 1 exactly, so q = roundf(x) on exact halves.
+    x = np.zeros(32, np.float32)
+    x[:8] = [127.0, 0.5, -0.5, 1.5, 2.5, -2.5, 126.5, -0.49999997]
+    q, d, s = orc.quantize_act(x[None])
+    assert d[0, 0] == np.float32(1.0)
+    assert list(q[0, :8]) == [127, 1, -1, 2, 3, -3, 127, 0]
+    assert s[0, 0] == 127 + 1 - 1 + 2 + 3 - 3 + 127 + 0
+    # amax = 254 gives d = 2 and 1/d = 0.5 (both exact): 3 -> 1.5 -> 2, 5 -> 2.5 -> 3, -1 -> -1
+    x = np.zeros(32, np.float32)
+    x[:4] = [-254.0, 3.0, 5.0, -1.0]
+    q, d, s = orc.quantize_act(x[None])
+    assert d[0, 0] == np.float32(2.0)
+    assert list(q[0, :4]) == [-127, 2, 3, -1]
+    assert s[0, 0] == -127 + 2 + 3 - 1
+
+
+def test_quantize_single_outlier_block(orc):
+    # one x20 outlier among ones: d = fp32(20/127), q_0 = 127, the ones map to round(127/20)=6
+    x = np.ones(32, np.float32)
+    x[5] = 20.0
+    q, d, s = orc.quantize_act(x[None])
+    assert d[0, 0] == np.float32(20.0) / np.float32(127.0)
+    assert q[0, 5] == 127 and (np.delete(q[0], 5) == 6).all()
+    assert s[0, 0] == 127 + 31 * 6
+
+
+def test_quantize_invariants_random(orc):
+    x = synth.make_activations(16, 1024, "pins", outliers=True)
+    q, d, s = orc.quantize_act(x)
+    xb = x.reshape(16, 32, 32).astype(np.float64)
+    qb = q.reshape(16, 32, 32).astype(np.int64)
+    assert np.abs(qb).max() <= 127
+    assert (np.abs(qb).max(axis=2) == 127).all()              # the block maximum maps to +-127
+    assert np.array_equal(s, qb.sum(axis=2))                    # exact block sums
+    amax = np.abs(xb).max(axis=2)
+    assert np.allclose(d, amax / 127.0, rtol=2 ** -23, atol=0)  # d is amax/127 to one rounding
+    err = np.abs(xb - d[:, :, None].astype(np.float64) * qb)   # reconstruction within half a step
+    assert (err <= d[:, :, None] * (0.5 + 1e-5)).all()
+    assert (np.sign(qb) * np.sign(xb) >= 0).all()
+
+
+# ---- integer block dots ----------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def golden_blocks():
+    with open(os.path.join(HERE, "golden", "one_block_dots.json")) as f:
+        return json.load(f)["cases"]
+
+
+def test_block_dots_hand_cases(orc, golden_blocks):
+    for case in golden_blocks:
+        fmt = synth.Q4 if case["fmt"] == "Q4" else synth.Q8
+        codes = np.array(case["w_codes"], np.int64).reshape(1, 32)
+        xq = np.array(case["x_codes"], np.int8).reshape(1, 32)
+        scale = np.array([[case["w_scale"]]], np.float16)
+        W = pack_q4(codes, scale) if fmt == synth.Q4 else pack_q8(codes, scale)
+        isum = orc.block_dots(W, 1, 32, fmt, xq)
+        assert isum[0, 0, 0] == case["isum"], case["name"]
+        xd = np.array([[case["x_scale"]]], np.float32)
+        y, A = orc.mmvq(W, 1, 32, fmt, xq, xd)
+        assert y[0, 0] == case["y"], case["name"]
+        assert A[0, 0] == abs(case["y"])
+
+
+@pytest.mark.parametrize("fmt", [synth.Q4, synth.Q8])
+def test_block_dots_brute_force(orc, fmt):
+    rng = np.random.default_rng(7)
+    rows, cols, T = 40, 256, 3
+    if fmt == synth.Q4:
+        codes = rng.integers(0, 16, (rows, cols))
+        W = pack_q4(codes, rng.random((rows, cols // 32)).astype(np.float16))
+        wv = codes - 8
+    else:
+        codes = rng.integers(-127, 128, (rows, cols))
+        W = pack_q8(codes, rng.random((rows, cols // 32)).astype(np.float16))
+        wv = codes
+    xq = rng.integers(-127, 128, (T, cols)).astype(np.int8)
+    got = orc.block_dots(W, rows, cols, fmt, xq)
+    ref = np.einsum("rbj,tbj->trb", wv.reshape(rows, cols // 32, 32).astype(np.int64),
+                    xq.reshape(T, cols // 32, 32).astype(np.int64))
+    assert np.array_equal(got, ref)
+
+
+# ---- fp64 GEMV -------------------------------------------------------------------------------------
+def dense_dequant(w: synth.Weights) -> np.ndarray:
+    codes = w.codes().astype(np.float64)
+    if w.fmt == synth.Q4:
+        codes -= 8.0
+    sc = np.repeat(w.scales.astype(np.float64), 32, axis=1)
+    return codes * sc
+
+
+@pytest.mark.parametrize("fmt,rows,cols,T", [(synth.Q4, 256, 512, 4), (synth.Q8, 96, 1024, 3),
+                                             (synth.Q4, 33, 96, 1)])
+def test_mmvq_brute_force_dense(orc, fmt, rows, cols, T):
+    w = synth.make_weights(rows, cols, fmt, "pin")
+    x = synth.make_activations(T, cols, "pin")
+    xq, xd, _ = orc.quantize_act(x)
+    y, A = orc.mmvq(w.buf, rows, cols, fmt, xq, xd)
+    xdeq = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
+    ref = xdeq @ dense_dequant(w).T                                  # [T][rows]
+    assert np.all(np.abs(y - ref) <= 1e-12 * A + 1e-300)
+    assert np.all(A >= np.abs(y))
+    ys, As = orc.mmvq_rows(w.buf, rows, cols, fmt, xq, xd, [rows - 1, 0, 5])
+    assert np.array_equal(ys, y[:, [rows - 1, 0, 5]]) and np.array_equal(As, A[:, [rows - 1, 0, 5]])
+
+
+def test_mmvq_linear_in_scales(orc):
+    # doubling every weight scale (exact in fp16) doubles every output exactly
+    w = synth.make_weights(64, 256, synth.Q4, "lin")
+    x = synth.make_activations(2, 256, "lin")
+    xq, xd, _ = orc.quantize_act(x)
+    y1, _ = orc.mmvq(w.buf, 64, 256, synth.Q4, xq, xd)
+    w2 = w.buf.copy()
+    sc = w2[w.plane_bytes:].view(np.float16)
+    sc *= np.float16(2.0)
+    y2, _ = orc.mmvq(w2, 64, 256, synth.Q4, xq, xd)
+    assert np.array_equal(y2, 2.0 * y1)
+
+
+# ---- argmax -----------------------------------------------------------------------------------------
+def test_argmax_ties_to_lowest(orc):
+    v = np.array([[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 5.0, 5.0], [-1.0, -2.0, -1.0, -1.5]])
+    assert list(orc.argmax(v)) == [1, 0, 0]
+    rng = np.random.default_rng(3)
+    r = rng.integers(0, 5, (6, 1000)).astype(np.float64)   # many ties
+    assert np.array_equal(orc.argmax(r), np.argmax(r, axis=1))
+
+
+def test_head_argmax_planted_tie(orc):
+    # rows 17 and 200 are byte-identical and every other row has scale 0 (logit exactly 0):
+    # the two equal maxima must resolve to the lower id, 17.
+    w = synth.make_weights(300, 256, synth.Q8, "tie")
+    nb = w.nb
+    buf = w.buf.copy()
+    buf[200 * nb * 32:201 * nb * 32] = buf[17 * nb * 32:18 * nb * 32]
+    sc = buf[w.plane_bytes:].view(np.float16).reshape(300, nb)
+    keep = sc[17].copy()
+    sc[:] = 0
+    sc[17] = keep
+    sc[200] = keep
+    x = synth.make_activations(1, 256, "tie")
+    xq, xd, _ = orc.quantize_act(x)
+    y, _ = orc.mmvq(buf, 300, 256, synth.Q8, xq, xd)
+    if y[0, 17] < 0:
+        xq = (-xq.astype(np.int16)).astype(np.int8)
+    ids, logits, _ = orc.head_argmax(buf, 300, 256, synth.Q8, xq, xd)
+    assert logits[0, 17] == logits[0, 200] > 0
+    assert ids[0] == 17
+
+
+# ---- MoE ---------------------------------------------------------------------------------------------
+def test_moe_bucket_matches_stable_sort(orc):
+    ids = synth.make_routing(300, 16, 4, "bucket")
+    counts, offsets, pairs, bad = orc.moe_bucket(ids, 16)
+    assert bad == 0
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    assert np.array_equal(pairs, order.astype(np.int32))
+    assert np.array_equal(counts, np.bincount(flat, minlength=16))
+    assert offsets[0] == 0 and np.array_equal(np.diff(offsets), counts)
+
+
+def test_moe_bucket_skips_bad_ids(orc):
+    ids = np.array([[0, 3], [-1, 1], [7, 0]], np.int32)
+    counts, offsets, pairs, bad = orc.moe_bucket(ids, 4)
+    assert bad == 2
+    assert list(counts) == [2, 1, 0, 1]
+    assert list(pairs[:4]) == [0, 5, 3, 1]
+
+
+def test_moe_rows_brute_force(orc):
+    n_exp, hidden, inter, n_tok, k = 4, 128, 64, 6, 2
+    experts = [(synth.make_weights(inter, hidden, synth.Q4, "g", e),
+                synth.make_weights(inter, hidden, synth.Q4, "u", e),
+                synth.make_weights(hidden, inter, synth.Q4, "d", e)) for e in range(n_exp)]
+    ids = synth.make_routing(n_tok, n_exp, k, "moe-bf")
+    x = synth.make_activations(n_tok, hidden, "moe-bf")
+    sel = np.arange(n_tok * k)
+    out = orc.moe_rows([(g.buf, u.buf, d.buf) for g, u, d in experts], hidden, inter, ids, x, sel,
+                       want_hidden=True)
+    xq, xd, _ = orc.quantize_act(x)
+    xdeq = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
+    for p in sel:
+        tok, e = p // k, ids.reshape(-1)[p]
+        g = dense_dequant(experts[e][0]) @ xdeq[tok]
+        u = dense_dequant(experts[e][1]) @ xdeq[tok]
+        h = g * u / (1.0 + np.exp(-g))
+        assert np.allclose(out["h"][p], h, rtol=1e-12, atol=1e-300)
+        hdeq = out["hq"][p].astype(np.float64) * np.repeat(out["hd"][p].astype(np.float64), 32)
+        yref = dense_dequant(experts[e][2]) @ hdeq
+        assert np.all(np.abs(out["y"][p] - yref) <= 1e-12 * out["A"][p] + 1e-300)
+    # the hidden re-quantization is the pinned quantizer applied to fp32(h)
+    q2, d2, s2 = orc.quantize_act(out["h"].astype(np.float32))
+    assert np.array_equal(q2, out["hq"]) and np.array_equal(d2, out["hd"]) and np.array_equal(s2, out["hs"])
+    # feeding the quantized hidden rows back reproduces y exactly
+    out2 = orc.moe_rows([(g.buf, u.buf, d.buf) for g, u, d in experts], hidden, inter, ids, x, sel,
+                        hq_in=out["hq"], hd_in=out["hd"])
+    assert np.array_equal(out2["y"], out["y"])
+
+
+def test_moe_rows_one_pair_equals_gemv(orc):
+    # one token routed to one expert: the row is the down GEMV of the re-quantized hidden row
+    hidden, inter = 64, 32
+    g, u, d = (synth.make_weights(inter, hidden, synth.Q4, "one", 0),
+               synth.make_weights(inter, hidden, synth.Q4, "one", 1),
+               synth.make_weights(hidden, inter, synth.Q4, "one", 2))
+    x = synth.make_activations(1, hidden, "one")
+    out = orc.moe_rows([(g.buf, u.buf, d.buf)], hidden, inter, np.zeros((1, 1), np.int32), x, [0],
+                       want_hidden=True)
+    y, A = orc.mmvq(d.buf, hidden, inter, synth.Q4, out["hq"], out["hd"])
+    assert np.array_equal(out["y"][0], y[0]) and np.array_equal(out["A"][0], A[0])
