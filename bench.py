@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-quantized verify window on GB300.
+
+One step = one full verify window (48 layers x {qkv, o, up, down} Q4 projections + the Q8 head
+GEMV and per-token argmax) at T tokens: quantize each projection's T input rows, run the T-column
+GEMV, finish with the head's argmax. The step is one CUDA graph replayed K times after W warm-up
+replays. Weights (1.52 GB) are larger than L2, so every step streams them from HBM.
+
+Prints ONE JSON line (rank 0). --impl reference times the CPU oracle instead (the reference arm).
+Multi-GPU: one process per GPU under torchrun; every rank runs its own independent windows
+(weak scaling, no collective on the data path); the timed region is bracketed by barriers and the
+maximum time over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-window tokens/s and weight GB/s (% of HBM roofline) at T=1/2/4/8"
+WORKLOAD = ("full verify window: 48 layers x {qkv 2048->5120, o 4096->2048, up 2048->6144, "
+            "down 6144->2048} Q4 + Q8 head 151936x2048 with per-token argmax")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="strata", choices=["strata", "reference"])
+    ap.add_argument("--T", type=int, default=4)
+    ap.add_argument("--layers", type=int, default=48)
+    ap.add_argument("--no-moe", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", default="window", choices=["window", "mmvq", "head", "moe"],
+                    help="window: the timed step; mmvq/head/moe: a few launches of one kernel (profiling)")
+    ap.add_argument("--rows", type=int, default=2048)
+    ap.add_argument("--cols", type=int, default=6144)
+    ap.add_argument("--fmt", type=int, default=0)
+    ap.add_argument("--reps", type=int, default=5)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---- CPU oracle baseline (bounded sample of the same workload) -------------------------------------
+class OracleSample:
+    """The oracle on a bounded sample of the window: the first layers' matrices and the head, each
+    over its first ``frac`` of rows, at T tokens. ``rate()`` scales the sample's time by its share
+    of the window's weight-times-token work to give the oracle's window tokens/s on this host."""
+
+    def __init__(self, T: int, layers: int, host_weights=None):
+        import oracle
+        from block_quantized_token_strata_gb300 import synth
+        oracle.build()
+        self.oracle, self.T = oracle, T
+        shapes = synth.window_shapes(layers)
+        idx = list(range(min(8, 4 * layers))) + [len(shapes) - 1]
+        self.total = sum(r * c for _, r, c, _ in shapes)
+        self.mats = []
+        for i in idx:
+            name, rows, cols, fmt = shapes[i]
+            w = host_weights[i] if host_weights is not None else synth.make_weights(rows, cols, fmt, "window", name)
+            x = synth.make_activations(T, cols, "window-x", name)
+            self.mats.append((name, w, rows, cols, fmt, x))
+
+    def run(self, frac: float) -> float:
+        """One pass over the sample; returns the fraction of the window's work it covered."""
+        o, part = self.oracle, 0
+        for name, w, rows, cols, fmt, x in self.mats:
+            n = max(1, int(rows * frac))
+            xq, xd, _ = o.quantize_act(x)
+            y, _ = o.mmvq_rows(w.buf, rows, cols, fmt, xq, xd, np.arange(n))
+            if name == "head":
+                o.argmax(y)
+            part += n * cols
+        return part / self.total
+
+    def calibrate(self, seconds: float) -> float:
+        t0 = time.perf_counter()
+        share = self.run(0.01)
+        el = max(time.perf_counter() - t0, 1e-4)
+        return float(min(1.0, max(0.001, 0.01 * seconds / el)))
+
+    def rate(self, seconds: float):
+        frac = self.calibrate(min(seconds, 5.0))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            share = self.run(frac)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        per_window = el / reps / share
+        desc = (f"first {frac:.2%} of the rows of {len(self.mats) - 1} layer matrices and of the head "
+                f"({share:.2%} of the window's weight x token work per pass), T={self.T}, {reps} passes")
+        return self.T / per_window, self.oracle.get_threads(), desc
+
+
+# ---- clocks ----------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---- reference arm -------------------------------------------------------------------------------------
+def run_reference(args, rank: int) -> None:
+    """The CPU oracle timed as it stands, each step a bounded sample sized so that the whole
+    --steps/--warmup run takes about two minutes."""
+    if rank != 0:
+        return
+    smp = OracleSample(args.T, args.layers)
+    per_step = max(0.05, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    frac = smp.calibrate(per_step)
+    for _ in range(args.warmup):
+        smp.run(frac)
+    times, share = [], None
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        share = smp.run(frac)
+        times.append(time.perf_counter() - t0)
+    per_window = statistics.median(times) / share
+    value = args.T / per_window
+    sample = (f"per step: first {frac:.2%} of the rows of 8 layer matrices and of the head "
+              f"({share:.2%} of the window's weight x token work), T={args.T}; time scaled to a full window")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_window,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": args.T, "layers": args.layers},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.oracle.get_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- GPU arm -------------------------------------------------------------------------------------------
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if args.case != "window":
+        run_case(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    from block_quantized_token_strata_gb300 import build, strata, synth
+    from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
+    build.build()
+    hbm_peak, peak_kind = peaks()
+
+    wts = WindowWeights(layers=args.layers, device="cuda", host_copy=(rank == 0 and not args.no_cpu))
+    T = args.T
+    wins = {t: VerifyWindow(wts, t) for t in sorted({1, 2, 4, 8, T})}
+    for w in wins.values():
+        w.load_inputs()
+    graphs = {t: w.capture() for t, w in wins.items()}
+    torch.cuda.synchronize()
+    launches = wins[T].launches_per_step()
+
+    # --- headline: K steps of the T-token window, device-resident inputs ---
+    g = graphs[T]
+    for _ in range(args.warmup):
+        g.replay()
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    barrier()
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if rank == 0 else 0.0)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms * 1e-3)
+
+    # --- per-T lines (same graph structure), weight GB/s ---
+    per_T = {}
+    for t, gg in graphs.items():
+        for _ in range(3):
+            gg.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(20, args.steps // 5)
+        a.record()
+        for _ in range(n):
+            gg.replay()
+        b.record()
+        torch.cuda.synchronize()
+        mt = a.elapsed_time(b) / n
+        gbs = wts.weight_bytes / (mt * 1e-3) / 1e9
+        per_T[str(t)] = {"ms_per_window": mt, "tokens_per_s": t / (mt * 1e-3), "weight_gbs": gbs,
+                         "hbm_frac": gbs / hbm_peak}
+
+    # --- roofline of the dominant kernel (the layer GEMVs): the same launches as the step, captured
+    # as two graphs (layers, head) so that CUDA events can bracket each part on the launching stream
+    win = wins[T]
+    n_mat = len(win.shapes)
+    g_lay, g_head = win.capture(0, n_mat - 1), win.capture(n_mat - 1, n_mat)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    lay, head = [], []
+    for i in range(max(20, args.steps // 10)):
+        ev[0].record()
+        g_lay.replay()
+        ev[1].record()
+        g_head.replay()
+        ev[2].record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            lay.append(ev[0].elapsed_time(ev[1]))
+            head.append(ev[1].elapsed_time(ev[2]))
+    n_gemv = len(win.shapes) - 1
+    layer_bytes = sum(synth.weight_nbytes(r, c, f) + T * c * 1.25 + T * r * 4 for _, r, c, f in win.shapes[:-1])
+    lay_ms = statistics.median(lay)
+    achieved = layer_bytes / (lay_ms * 1e-3) / 1e9
+    _, vr, vc, vf = win.shapes[-1]
+    head_bytes = synth.weight_nbytes(vr, vc, vf) + T * vc * 1.25
+    head_ms = statistics.median(head)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": None,
+                "kernel": "mmvq_kernel<Q4,T> (192 layer GEMV launches per window)",
+                "bytes_per_launch": layer_bytes / n_gemv, "us_per_launch": lay_ms * 1e3 / n_gemv,
+                "peak_kind": peak_kind,
+                "note": "per-launch time = layer section / 192, which also holds the 192 interleaved quantize launches",
+                "head": {"gbs": head_bytes / (head_ms * 1e-3) / 1e9, "us": head_ms * 1e3}}
+
+    # --- end to end through the public API: pinned host inputs in, ids out, every step ---
+    x_host = torch.from_numpy(win.host_inputs()).pin_memory()
+    ids_host = torch.empty(T, dtype=torch.int32).pin_memory()
+    for _ in range(3):
+        win.run_host(graphs[T], x_host, ids_host)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(20, args.steps // 5)
+    t_wall = time.perf_counter()
+    a.record()
+    for _ in range(n_e2e):
+        win.run_host(graphs[T], x_host, ids_host)
+    b.record()
+    barrier()
+    wall = (time.perf_counter() - t_wall) / n_e2e
+    e2e_ms = a.elapsed_time(b) / n_e2e
+    e2e = {"value": world * T / (max(e2e_ms, wall * 1e3) * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(T * 4)}
+
+    # --- prompt-chunk MoE (grouped experts), reported beside the window ---
+    moe = None
+    if not args.no_moe:
+        moe = bench_moe(torch, strata, synth, args)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, cores, sample = OracleSample(T, args.layers, wts.host).rate(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 dots (dp4a, exact int32) + fp32 scale/accumulate",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T, "layers": args.layers,
+                       "weight_bytes_per_window": wts.weight_bytes,
+                       "l2": "inputs larger than L2 (1.52 GB of weights per step)",
+                       "graph": "one CUDA graph per window, programmatic dependent launch between kernels"},
+            "weight_gbs": wts.weight_bytes / (ms * 1e-3) / 1e9 * world,
+            "hbm_frac": wts.weight_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+            "per_T": per_T, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_moe(torch, strata, synth, args, reps=20):
+    """One prompt chunk of the MoE experts (3,256 tokens, 128 experts, top-8), CUDA graph replays."""
+    E, H, I, N, K = synth.MOE_EXPERTS, synth.MOE_HIDDEN, synth.MOE_INTER, synth.MOE_TOKENS, synth.MOE_TOPK
+    dev = [tuple(torch.from_numpy(synth.make_weights(r, c, synth.Q4, "prompt-moe", w, e).buf).cuda()
+                 for w, r, c in (("g", I, H), ("u", I, H), ("d", H, I))) for e in range(E)]
+    tab = strata.expert_table(dev, "cuda")
+    ids = torch.from_numpy(synth.make_routing(N, E, K, "prompt-moe")).cuda()
+    x = torch.from_numpy(synth.make_activations(N, H, "prompt-moe")).cuda()
+    y = torch.empty((N * K, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(strata.moe_grouped_workspace(E, N, K, H, I), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        strata.moe_grouped(tab, E, H, I, ids, x, y=y, workspace=ws, err_word=err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = reps
+    a.record()
+    for _ in range(n):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    ops = 2.0 * N * K * (2 * I * H + H * I)
+    return {"workload": "3,256 tokens x top-8 of 128 experts, Q4 gate/up 2048->768, down 768->2048",
+            "ms_per_chunk": ms, "tokens_per_s": N / (ms * 1e-3), "int8_tops": ops / (ms * 1e-3) / 1e12,
+            "err_word": int(err.item())}
+
+
+def run_case(args):
+    """A few plain launches of one kernel on one workload (for profilers); prints its mean time."""
+    import torch
+    from block_quantized_token_strata_gb300 import build, strata, synth
+    build.build()
+    torch.cuda.set_device(0)
+    T = args.T
+    if args.case in ("mmvq", "head"):
+        rows = synth.HEAD_VOCAB if args.case == "head" else args.rows
+        cols = synth.WINDOW_HIDDEN if args.case == "head" else args.cols
+        fmt = synth.Q8 if args.case == "head" else args.fmt
+        W = torch.from_numpy(synth.make_weights(rows, cols, fmt, "case").buf).cuda()
+        xq, xd, xs = strata.quantize_act(torch.from_numpy(synth.make_activations(T, cols, "case")).cuda())
+        y = torch.empty((T, rows), dtype=torch.float32, device="cuda")
+        ids = torch.empty(T, dtype=torch.int32, device="cuda")
+        ws = torch.empty(strata.head_argmax_workspace(rows, T), dtype=torch.uint8, device="cuda")
+
+        def step():
+            if args.case == "head":
+                strata.head_argmax(W, rows, cols, fmt, xq, xd, xs, T, ids, None, ws)
+            else:
+                strata.mmvq_multi(W, rows, cols, fmt, xq, xd, xs, T, y)
+        nbytes = synth.weight_nbytes(rows, cols, fmt)
+    else:
+        out = bench_moe(torch, strata, synth, args, reps=args.reps)
+        print(json.dumps({"case": "moe", **out}))
+        return
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.reps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.reps
+    print(json.dumps({"case": args.case, "rows": rows, "cols": cols, "fmt": fmt, "T": T, "us": ms * 1e3,
+                      "weight_gbs": nbytes / (ms * 1e-3) / 1e9}))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,111 @@
+"""The C-ABI library loads, exports every call include/strata.h declares, and rejects bad arguments
+on the host with the documented status codes (no GPU needed: a rejected call launches nothing)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_quantized_token_strata_gb300 import build as strata_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "strata.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    strata_build.build()
+    from block_quantized_token_strata_gb300 import strata
+    return strata.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(strata_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_error_strings(L):
+    for code in range(0, -9, -1):
+        s = L.strata_error_string(code)
+        assert s and s != b"unknown status"
+    assert L.strata_error_string(-99) == b"unknown status"
+
+
+def test_weight_bytes(L):
+    assert L.strata_weight_bytes(4096, 4096, 0) == 4096 * 128 * 18
+    assert L.strata_weight_bytes(151936, 2048, 1) == 151936 * 64 * 34
+    assert L.strata_weight_bytes(4, 33, 0) == 0
+    assert L.strata_weight_bytes(4, 64, 9) == 0
+
+
+A16 = 0x10000  # fake, aligned, never dereferenced: every call below fails its host checks first
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 2048, 2048, 0, A16, A16, A16, 4, A16, None), -1),        # W NULL
+    ((A16, 2048, 2048, 0, 0, A16, A16, 4, A16, None), -1),        # xq NULL
+    ((A16, 2048, 2000, 0, A16, A16, A16, 4, A16, None), -2),      # cols % 32
+    ((A16, 0, 2048, 0, A16, A16, A16, 4, A16, None), -2),         # rows 0
+    ((A16, 2048, 2048, 0, A16, A16, A16, 0, A16, None), -3),      # T 0
+    ((A16, 2048, 2048, 0, A16, A16, A16, 9, A16, None), -3),      # T 9
+    ((A16, 2048, 2048, 5, A16, A16, A16, 4, A16, None), -4),      # fmt
+    ((A16 + 8, 2048, 2048, 0, A16, A16, A16, 4, A16, None), -7),  # W misaligned
+    ((A16, 2048, 2048, 0, A16 + 4, A16, A16, 4, A16, None), -7),  # xq misaligned
+    ((A16, 2048, 65536, 0, A16, A16, A16, 4, A16, None), -2),     # T*cols above the staged maximum
+])
+def test_mmvq_rejects(L, args, code):
+    assert L.strata_mmvq_multi(*args) == code
+
+
+def test_quantize_rejects(L):
+    assert L.strata_quantize_act(0, 4, 64, A16, A16, A16, None) == -1
+    assert L.strata_quantize_act(A16, 4, 40, A16, A16, A16, None) == -2
+    assert L.strata_quantize_act(A16, 0, 64, A16, A16, A16, None) == -2
+    assert L.strata_quantize_act(A16 + 4, 4, 64, A16, A16, A16, None) == -7
+
+
+def test_head_rejects(L):
+    ws = L.strata_head_argmax_workspace(151936, 4)
+    assert ws > 0 and L.strata_head_argmax_workspace(151936, 9) == 0
+    ok = (A16, 151936, 2048, 1, A16, A16, A16, 4, A16, None, A16, ws, None)
+    bad_ws = ok[:10] + (A16, ws - 1, None)
+    assert L.strata_head_argmax(*bad_ws) == -8
+    no_ws = ok[:10] + (None, ws, None)
+    assert L.strata_head_argmax(*no_ws) == -8
+    no_ids = ok[:8] + (None,) + ok[9:]
+    assert L.strata_head_argmax(*no_ids) == -1
+    badT = ok[:7] + (0,) + ok[8:]
+    assert L.strata_head_argmax(*badT) == -3
+
+
+def test_moe_rejects(L):
+    ws = L.strata_moe_grouped_workspace(128, 3256, 8, 2048, 768)
+    assert ws > 3256 * 8 * 768
+    assert L.strata_moe_grouped_workspace(128, 3256, 8, 2000, 768) == 0
+    ok = [A16, 128, 2048, 768, A16, 3256, 8, A16, A16, A16, ws, None, None]
+    a = list(ok); a[0] = None
+    assert L.strata_moe_grouped(*a) == -1
+    a = list(ok); a[2] = 2000
+    assert L.strata_moe_grouped(*a) == -2
+    a = list(ok); a[6] = 17
+    assert L.strata_moe_grouped(*a) == -2
+    a = list(ok); a[10] = ws - 1
+    assert L.strata_moe_grouped(*a) == -8
+    a = list(ok); a[9] = A16 + 16
+    assert L.strata_moe_grouped(*a) == -7
+
+
+def test_moe_debug_views(L):
+    out = (ctypes.c_size_t * 7)()
+    assert L.strata_moe_debug_views(128, 3256, 8, 2048, 768, ctypes.cast(out, ctypes.c_void_p)) == 0
+    vals = list(out)
+    assert vals == sorted(vals) and all(v % 256 == 0 for v in vals)
+    assert vals[6] == L.strata_moe_grouped_workspace(128, 3256, 8, 2048, 768)
