@@ -369,6 +369,15 @@ static int head_grid_bound(int64_t vocab)
     return int(want < 4096 ? want : 4096);
 }
 
+// scratch bytes one head launch uses on the current device (same grid formula as launch_t for R=4)
+size_t head_launch_scratch_bytes(int64_t vocab, int T)
+{
+    const int64_t rg = (vocab + 3) / 4;
+    const int64_t want = (rg + kWarps - 1) / kWarps;
+    const int64_t cap = int64_t(device_sm_count()) * 4;
+    return size_t(want < cap ? want : cap) * size_t(T) * 8;
+}
+
 size_t head_workspace_bytes(int64_t vocab, int T)
 {
     return size_t(head_grid_bound(vocab)) * size_t(T) * 8 + 256;

@@ -134,6 +134,22 @@ int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt,
                        cudaStream_t stream);
 
 /*
+ * strata_head_argmax_noalloc — strata_head_argmax for callers that cannot allocate device memory.
+ *   The pages have no counterpart: this entry point exists for callers such as plugins inside a
+ *   host application that owns all device memory, or servers that fix their memory at start-up,
+ *   which cannot provide the workspace strata_head_argmax asks for. Same arguments, layouts and
+ *   results as strata_head_argmax minus the workspace; the per-CTA argmax candidates live in a
+ *   64 KiB array inside the library, held on every device that loads it until the process exits.
+ *   It allocates nothing and calls no allocating routine. Its first call on a device looks up the
+ *   array's device address (make that first call before any stream capture). All calls share the
+ *   array: calls that overlap on the GPU race on it. Returns STRATA_ERR_WORKSPACE when a launch
+ *   would need more than the 64 KiB; otherwise the errors of strata_head_argmax.
+ */
+int strata_head_argmax_noalloc(const void* W, int64_t vocab, int64_t cols, int fmt,
+                               const int8_t* xq, const float* xd, const int32_t* xs, int T,
+                               int32_t* ids, float* logits, cudaStream_t stream);
+
+/*
  * strata_moe_grouped — prompt-chunk MoE experts: per (token, slot) pair p = tok*k + slot routed to
  * expert e = ids[p]:
  *     g = W_gate[e] . xq(tok), u = W_up[e] . xq(tok)         (block arithmetic above, fp32)
