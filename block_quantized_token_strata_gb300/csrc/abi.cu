@@ -74,9 +74,38 @@ int strata_mmvq_multi(const void* W, int64_t rows, int64_t cols, int fmt, const 
     st = check_matrix(rows, cols, fmt);
     if (st != STRATA_OK) return st;
     if (T < 1 || T > STRATA_MAX_T) return STRATA_ERR_T;
-    if (int64_t(T) * cols > kMaxStagedTCols) return STRATA_ERR_SHAPE;
+    if (int64_t(T) * cols > kMaxStagedTCols || !gemv_shape_fits(cols, fmt, T)) return STRATA_ERR_SHAPE;
     if (!aligned(W, 16) || !aligned(y, 4)) return STRATA_ERR_ALIGN;
     return cuda_status(launch_mmvq(W, rows, cols, fmt, xq, xd, xs, T, y, stream));
+}
+
+int strata_mmvq_grouped(const strata_gemv_desc* descs, int n, int fmt, int T, cudaStream_t stream)
+{
+    if (!descs) return STRATA_ERR_NULL;
+    if (n < 1 || n > kMaxGroupedMatrices) return STRATA_ERR_SHAPE;
+    if (fmt != STRATA_Q4 && fmt != STRATA_Q8) return STRATA_ERR_FMT;
+    if (T < 1 || T > STRATA_MAX_T) return STRATA_ERR_T;
+    int64_t cols_max = 0, total_rows = 0;
+    for (int i = 0; i < n; ++i) {
+        const strata_gemv_desc& d = descs[i];
+        if (!d.W || !d.y) return STRATA_ERR_NULL;
+        int st = check_acts(d.xq, d.xd, d.xs);
+        if (st != STRATA_OK) return st;
+        st = check_matrix(d.rows, d.cols, fmt);
+        if (st != STRATA_OK) return st;
+        if (int64_t(T) * d.cols > kMaxStagedTCols || !gemv_shape_fits(d.cols, fmt, T)) return STRATA_ERR_SHAPE;
+        if (!aligned(d.W, 16) || !aligned(d.y, 4)) return STRATA_ERR_ALIGN;
+        cols_max = d.cols > cols_max ? d.cols : cols_max;
+        total_rows += d.rows;
+    }
+    if (!gemv_shape_fits(cols_max, fmt, T) || total_rows > (int64_t(1) << 30)) return STRATA_ERR_SHAPE;
+    return cuda_status(launch_mmvq_grouped(descs, n, fmt, T, stream));
+}
+
+int strata_device_error(int* out, int clear)
+{
+    if (!out) return STRATA_ERR_NULL;
+    return cuda_status(read_device_error(out, clear != 0));
 }
 
 size_t strata_head_argmax_workspace(int64_t vocab, int T)
@@ -95,7 +124,7 @@ int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, cons
     st = check_matrix(vocab, cols, fmt);
     if (st != STRATA_OK) return st;
     if (T < 1 || T > STRATA_MAX_T) return STRATA_ERR_T;
-    if (int64_t(T) * cols > kMaxStagedTCols) return STRATA_ERR_SHAPE;
+    if (int64_t(T) * cols > kMaxStagedTCols || !gemv_shape_fits(cols, fmt, T)) return STRATA_ERR_SHAPE;
     if (!aligned(W, 16) || !aligned(ids, 4) || (logits && !aligned(logits, 4))) return STRATA_ERR_ALIGN;
     if (!workspace || ws_bytes < head_workspace_bytes(vocab, T)) return STRATA_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return STRATA_ERR_ALIGN;

@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <utility>
 
+#include "strata.h"
+
 namespace strata {
 
 // Launch with programmatic stream serialization: the kernel may start while the previous kernel on
@@ -40,6 +42,16 @@ size_t head_launch_scratch_bytes(int64_t vocab, int T);  // bytes one launch use
 cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq,
                                const float* xd, const int32_t* xs, int T, int32_t* ids, float* logits,
                                void* workspace, cudaStream_t stream);
+
+// many independent matrices of one format in one persistent launch
+cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T, cudaStream_t stream);
+constexpr int kMaxGroupedMatrices = 192;
+// warps per row of the GEMV for a shape (fixes the fp32 summation order; independent of T)
+int gemv_warps_per_row(int64_t cols, int fmt);
+// whether the shared-memory plan of a shape fits at T
+bool gemv_shape_fits(int64_t cols, int fmt, int T);
+// device error word: bit 0 = a bounded wait in a kernel ran out
+cudaError_t read_device_error(int* out, bool clear);
 
 cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq,
                               const int32_t* xs, int T, int32_t* isum, cudaStream_t stream);

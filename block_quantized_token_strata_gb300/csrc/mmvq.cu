@@ -1,208 +1,443 @@
-// mmvq.cu — multi-token block-quantized GEMV (T <= 8 columns, one weight read) and the fused
-// vocabulary head + argmax.
+// mmvq.cu — multi-token block-quantized GEMV (T <= 8 columns, one weight read), its grouped form
+// (many independent matrices in one persistent launch) and the fused vocabulary head + argmax.
 //
 // What it computes: y[t][r] = sum_b (d_w[r][b] * d_x[t][b]) * isum[t][r][b] with exact int32 block
 // dots isum, for T tokens that share one read of W — the verify window's "multi-column MMVQ in
 // exact mode" (Strata commit "wire multi-token kernels into Verifier and MtpDrafter CUDA graphs",
 // verify.hpp header comment). As in the hoisted-load MMVQ-IL kernels of the pull request "sm_80
-// (GA100) tuning", the integer dots are exact, the int->float conversion is the exact
-// 1.5*2^23 magic form, and the fp32 accumulation order and the xor tree are fixed.
+// (GA100) tuning", the integer dots are exact, the int->float conversion is the exact 1.5*2^23
+// magic form, and the fp32 accumulation order and the xor tree are fixed.
 //
-// Exactness across T (column t of a T-token launch == the T = 1 launch):
-//   * lane l of the warp that owns row r takes blocks b = l, l+32, l+64, ... in ascending order and
-//     folds each into acc = fma(d_w*d_x, float(isum), acc) with explicitly rounded intrinsics;
-//   * the 32 lane partials are combined by the xor tree 16, 8, 4, 2, 1;
-//   * neither the lane<->block map nor the tree depends on T, R (rows a warp holds at once), the
-//     grid or the CTA size; T is only the trip count of an inner loop over independent columns.
+// Exactness across T (column t of a T-token launch == the T = 1 launch), by construction:
+//   * a row is owned by KS warps (G = 32*KS lanes); KS is a function of (cols, fmt) only;
+//   * lane g (0 <= g < G) folds blocks b = g, g+G, g+2G, ... in ascending order into
+//     acc = fma(d_w*d_x, float(isum), acc) with explicitly rounded intrinsics;
+//   * each warp combines its 32 partials in the xor order 16, 8, 4, 2, 1 (done as a butterfly
+//     reduce-scatter, which performs exactly the same pairwise additions for every value), then
+//     the KS warp sums are added in warp order;
+//   * T only sets the trip count of loops over independent columns. Nothing else depends on it.
 //
-// Data movement (GB300): W streams from HBM with 128-bit read-only loads that skip L1; before the
-// kernel waits on its predecessor (programmatic dependent launch) each CTA issues bulk L2
-// prefetches for the first rows of its contiguous row range, and every warp keeps prefetching a
-// fixed distance ahead, so the HBM queue is full while the previous kernel drains. Activations
-// (T x cols codes, scales, sums) are staged once per CTA in shared memory, split into the 16-byte
-// halves each dp4a chain consumes so that lanes read consecutive 16-byte words (no conflicts).
+// Data movement (GB300): a producer warp streams each CTA's contiguous rows with bulk (TMA) copies
+// into a ring of shared-memory slots, one row group of four rows per slot, completion tracked by
+// mbarriers; it starts before the kernel waits on its predecessor (programmatic dependent launch),
+// so weight bytes are in flight while the previous kernel finishes. Eight consumer warps read
+// codes and scales from the slots (consecutive lanes, consecutive 16-byte words) and the T
+// activation columns from a shared-memory copy made once per matrix, laid out as the 16-byte
+// halves each dp4a chain consumes. Every wait is bounded; a timeout sets the device error word.
 #include <float.h>
 #include <limits.h>
+
+#include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace strata {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+constexpr int kR = 4;                     // rows per row group (= per ring slot)
+constexpr int kMaxGroup = 192;            // matrices per grouped launch
+constexpr int kMaxGrid = 1024;
+constexpr int kCtasPerSm = 1;             // resident CTAs per SM the launch plans for
+
+// bit 0: a bounded wait ran out; bit 1: the producer waiting for a free stage; bit 2: a consumer
+// waiting for a stage's bytes; bit 3: the producer draining its last copies
+__device__ int g_strata_device_error = 0;
 
 template <int FMT> struct FmtInfo;
 template <> struct FmtInfo<0> { static constexpr int kQB = 16; };  // Q4: 16 code bytes per block
 template <> struct FmtInfo<1> { static constexpr int kQB = 32; };  // Q8: 32 code bytes per block
 
-struct MmvqArgs {
+struct GemvMat {
     const uint8_t* W;
-    int rows;
-    int nb;
     const int8_t* xq;
     const float* xd;
     const int32_t* xs;
-    float* y;          // [T][rows] or null
-    float* cand_val;   // head: [T][gridDim.x] per-CTA maxima
-    int* cand_idx;     // head: [T][gridDim.x] their row ids
-    int rg_total;      // row groups of R rows
-    int pf_rg;         // prefetch distance in row groups
+    float* y;
+    int rows, nb, ks;
+    int sg;      // chunks (row groups) per ring stage
+    int chunk0;  // first chunk of this matrix in the launch's chunk sequence
+};
+
+template <int MAXM>
+struct GemvParams {
+    int n_mat;
+    int n_chunk;     // row groups over all matrices
+    int cstage;      // bytes per stage in the code ring (multiple of 128)
+    int sstage;      // bytes per stage in the scale ring (multiple of 128, 32 bytes of slack)
+    int ns;          // stages in the ring
+    int nb_max;      // widest matrix, for the activation copy
+    int pf;          // stages the producer prefetches into L2 ahead of its bulk copies
+    float* cand_val; // head: [T][gridDim.x] per-CTA maxima
+    int* cand_idx;   // head: [T][gridDim.x] their row ids
+    int plan[MAXM > 1 ? kMaxGrid + 1 : 1];  // grouped: first chunk of each CTA (and the end)
+    GemvMat m[MAXM];
 };
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-template <int FMT, int T, int R, bool HEAD>
-__global__ void __launch_bounds__(kThreads, 2) mmvq_kernel(const MmvqArgs a)
+// V values per lane -> after the five xor levels lane l holds the full sum of value vidx(l).
+template <int V>
+__device__ __forceinline__ float butterfly(float (&v)[V], int lane, int& vidx) {
+    vidx = 0;
+#pragma unroll
+    for (int lvl = 0; lvl < 5; ++lvl) {
+        const int o = 16 >> lvl;
+        const int c = (V >> lvl) > 1 ? (V >> lvl) : 1;  // values still held before this level
+        if (c > 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int q = 0; q < c / 2; ++q) {
+                const float send = up ? v[q] : v[q + c / 2];
+                const float keep = up ? v[q + c / 2] : v[q];
+                v[q] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+            vidx += up ? c / 2 : 0;
+        } else {
+            v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+        }
+    }
+    return v[0];
+}
+
+template <int N> struct Pow2Ceil { static constexpr int v = N <= 1 ? 1 : 2 * Pow2Ceil<(N + 1) / 2>::v; };
+template <> struct Pow2Ceil<1> { static constexpr int v = 1; };
+
+// Walks a CTA's chunks [g0, g1) as stages: within each matrix, runs of `sg` consecutive row groups
+// (about 32 KB), so that one bulk copy moves a whole stage.
+template <int MAXM>
+struct StageIter {
+    const GemvParams<MAXM>* p;
+    int g1, mi, sg, se, send;  // matrix, stage start, stage end, end of the matrix's run
+    __device__ void init(const GemvParams<MAXM>& prm, int g0, int gend) {
+        p = &prm;
+        g1 = gend;
+        mi = 0;
+        if constexpr (MAXM > 1) {
+            while (mi + 1 < prm.n_mat && prm.m[mi + 1].chunk0 <= g0) ++mi;
+        }
+        sg = g0;
+        settle();
+    }
+    __device__ void settle() {
+        if constexpr (MAXM > 1) {
+            while (mi + 1 < p->n_mat && p->m[mi + 1].chunk0 <= sg) ++mi;
+        }
+        const int mend = (MAXM > 1 && mi + 1 < p->n_mat) ? p->m[mi + 1].chunk0 : p->n_chunk;
+        send = min(g1, mend);
+        se = min(sg + p->m[mi].sg, send);
+    }
+    __device__ bool valid() const { return sg < g1; }
+    __device__ void next() { sg = se; if (sg < g1) settle(); }
+};
+
+template <int FMT, int T, int MAXM, bool HEAD>
+__global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<MAXM> p)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
     constexpr int QB = FmtInfo<FMT>::kQB;
-    constexpr int QV = QB / 16;  // 16-byte code words per block
-    const int nb = a.nb;
-    const int rows = a.rows;
-    uint4* sx = reinterpret_cast<uint4*>(smem);                               // [T][2][nb]
-    int2* scd = reinterpret_cast<int2*>(smem + size_t(T) * 2 * nb * 16);     // [T][nb] (c0, d_x)
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    constexpr int QV = QB / 16;
+    constexpr int V = Pow2Ceil<kR * T>::v;
+    constexpr int TPP = T <= 2 ? 2 : (T <= 4 ? 4 : 8);  // tokens padded for the scale vectors
+    constexpr int NP = (T + 1) / 2;                      // token pairs
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ volatile int s_abort;
 
-    const int rg0 = int((int64_t(blockIdx.x) * a.rg_total) / gridDim.x);
-    const int rg1 = int((int64_t(blockIdx.x + 1) * a.rg_total) / gridDim.x);
-    const uint8_t* qplane = a.W;
-    const unsigned short* splane =
-        reinterpret_cast<const unsigned short*>(a.W + size_t(rows) * nb * QB);
+    const int NST = p.ns;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                 // full[NST], empty[NST]
+    uint8_t* xsm = smem + 2 * 8 * 32;                                    // activations
+    float* red = reinterpret_cast<float*>(xsm + size_t(p.nb_max) * (T * 32 + TPP * 8));  // [2][kCW][32]
+    float* hv = red + 2 * kCW * 32;                                      // head: [kCW*32] values
+    int* hi = reinterpret_cast<int*>(hv + kCW * 32);                     // head: [kCW*32] ids
+    uint8_t* cring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(hi + kCW * 32) + 127) & ~uintptr_t(127));   // codes [NST][cstage]
+    uint8_t* sring = cring + size_t(NST) * p.cstage;                              // scales [NST][sstage]
 
-    auto prefetch_groups = [&](int g0, int g1) {  // row groups [g0, g1) of this matrix
-        const int r0 = g0 * R;
-        const int r1 = min(g1 * R, rows);
-        if (r0 >= r1) return;
-        prefetch_l2(qplane + size_t(r0) * nb * QB, size_t(r1 - r0) * nb * QB);
-        prefetch_l2(splane + size_t(r0) * nb, size_t(r1 - r0) * nb * 2);
-    };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int g0, g1;  // this CTA's chunks
+    if constexpr (MAXM > 1) {
+        g0 = p.plan[blockIdx.x];
+        g1 = p.plan[blockIdx.x + 1];
+    } else {
+        g0 = int((int64_t(blockIdx.x) * p.n_chunk) / gridDim.x);
+        g1 = int((int64_t(blockIdx.x + 1) * p.n_chunk) / gridDim.x);
+    }
 
-    // (1) weights are static data: start pulling this CTA's first rows toward L2 now
-    if (threadIdx.x == 0) prefetch_groups(rg0, min(rg1, rg0 + a.pf_rg));
-
-    // (2) activations may come from the previous kernel: wait, then let the next one start
-    pdl_wait();
-    pdl_launch();
-
-    {
-        const int nchunk = T * nb * 2;
-        const uint4* src = reinterpret_cast<const uint4*>(a.xq);
-        for (int i = threadIdx.x; i < nchunk; i += kThreads) {
-            const int t = i / (2 * nb);
-            const int c = i - t * 2 * nb;
-            sx[(t * 2 + (c & 1)) * nb + (c >> 1)] = __ldg(src + i);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);           // full: the producer's expect_tx arrival
+            mbar_init(smem_u32(&bars[NST + s]), kCW);   // empty: one arrival per consumer warp
         }
-        for (int i = threadIdx.x; i < T * nb; i += kThreads) {
-            const int c0 = (FMT == 0) ? kMagicBits - 8 * __ldg(a.xs + i) : kMagicBits;
-            scd[i] = make_int2(c0, __float_as_int(__ldg(a.xd + i)));
-        }
+        s_abort = 0;
+        mbar_fence_init();
     }
     __syncthreads();
 
-    float best[HEAD ? T : 1];
-    int bidx[HEAD ? T : 1];
-    if constexpr (HEAD) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) { best[t] = -FLT_MAX; bidx[t] = INT_MAX; }
-    }
-
-    for (int rg = rg0 + warp; rg < rg1; rg += kWarps) {
-        if (lane == 0 && rg + a.pf_rg < rg1) prefetch_groups(rg + a.pf_rg, rg + a.pf_rg + 1);
-        const int row0 = rg * R;
-        const uint8_t* wr[R];
-        const unsigned short* sr[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int rr = min(row0 + r, rows - 1);
-            wr[r] = qplane + size_t(rr) * nb * QB;
-            sr[r] = splane + size_t(rr) * nb;
-        }
-        float acc[R][T];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int t = 0; t < T; ++t) acc[r][t] = 0.0f;
-
-        for (int kb0 = lane; kb0 < nb; kb0 += 64) {
-            const int kb1 = kb0 + 32;
-            const bool has1 = kb1 < nb;
-            uint4 w[2][R][QV];
-            float dw[2][R];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int kb = u ? (has1 ? kb1 : kb0) : kb0;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-#pragma unroll
-                    for (int h = 0; h < QV; ++h) w[u][r][h] = ld_stream_v4(wr[r] + size_t(kb) * QB + h * 16);
-                    dw[u][r] = __half2float(__ushort_as_half(ld_stream_u16(sr[r] + kb)));
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                if (u == 1 && !has1) break;
-                const int kb = u ? kb1 : kb0;
-#pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    const uint4 xl = sx[(t * 2 + 0) * nb + kb];
-                    const uint4 xh = sx[(t * 2 + 1) * nb + kb];
-                    const int2 cd = scd[t * nb + kb];
-                    const float dx = __int_as_float(cd.y);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        int c;
-                        if constexpr (FMT == 0) c = dot_q4(w[u][r][0], xl, xh, cd.x);
-                        else c = dot_q8(w[u][r][0], w[u][r][QV - 1], xl, xh, cd.x);
-                        const float f = magic_to_float(c);
-                        const float s = __fmul_rn(dw[u][r], dx);
-                        acc[r][t] = __fmaf_rn(s, f, acc[r][t]);
-                    }
-                }
-            }
-        }
-
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = row0 + r;
-#pragma unroll
-            for (int t = 0; t < T; ++t) {
-                float v = acc[r][t];
-                v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 16));
-                v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 8));
-                v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
-                v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
-                v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
-                if (row < rows) {
-                    if (a.y != nullptr && lane == ((r * T + t) & 31)) a.y[size_t(t) * rows + row] = v;
-                    if constexpr (HEAD) {
-                        if (better(v, row, best[t], bidx[t])) { best[t] = v; bidx[t] = row; }
-                    }
-                }
-            }
-        }
-    }
-
-    if constexpr (HEAD) {
-        float* rv = reinterpret_cast<float*>(scd + T * nb);   // [kWarps][T]
-        int* ri = reinterpret_cast<int*>(rv + kWarps * T);
+    // ------------------------------------------------------------------ producer warp
+    if (warp == kCW) {
         if (lane == 0) {
-#pragma unroll
-            for (int t = 0; t < T; ++t) { rv[warp * T + t] = best[t]; ri[warp * T + t] = bidx[t]; }
+            const uint64_t pol = policy_evict_first();
+            StageIter<MAXM> it, pf;
+            it.init(p, g0, g1);
+            pf.init(p, g0, g1);
+            // L2 prefetch runs p.pf stages ahead of the bulk copies, so that they find their bytes in
+            // L2 rather than waiting out HBM latency under load.
+            auto prefetch_next = [&]() {
+                if (!pf.valid()) return;
+                const GemvMat& m = p.m[pf.mi];
+                const int r0 = (pf.sg - m.chunk0) * kR;
+                const int nr = min((pf.se - pf.sg) * kR, m.rows - r0);
+                bulk_prefetch_l2(m.W + size_t(r0) * m.nb * QB, uint32_t(nr) * m.nb * QB);
+                const uintptr_t sa = reinterpret_cast<uintptr_t>(m.W + size_t(m.rows) * m.nb * QB + size_t(r0) * m.nb * 2);
+                const uintptr_t lo = (sa + 15) & ~uintptr_t(15), hi2 = (sa + uint32_t(nr) * m.nb * 2) & ~uintptr_t(15);
+                if (hi2 > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), uint32_t(hi2 - lo));
+                pf.next();
+            };
+            for (int k = 0; k < p.pf; ++k) prefetch_next();
+            bool waited = false;
+            int k = 0;
+            for (; it.valid(); it.next(), ++k) {
+                const int s = k % NST;
+                if (k == NST) {  // the ring is full: from here on, order after the predecessor
+                    pdl_wait();
+                    pdl_launch();
+                    waited = true;
+                }
+                if (k >= NST) {
+                    if (!mbar_wait(smem_u32(&bars[NST + s]), ((k / NST) - 1) & 1, &s_abort)) {
+                        s_abort = 1;
+                        atomicOr(&g_strata_device_error, 1 | 2);
+                        break;
+                    }
+                }
+                prefetch_next();
+                const GemvMat& m = p.m[it.mi];
+                const int r0 = (it.sg - m.chunk0) * kR;
+                const int nr = min((it.se - it.sg) * kR, m.rows - r0);
+                const uint8_t* qsrc = m.W + size_t(r0) * m.nb * QB;
+                const uint32_t qbytes = uint32_t(nr) * m.nb * QB;
+                const uint8_t* ssrc = m.W + size_t(m.rows) * m.nb * QB + size_t(r0) * m.nb * 2;
+                const uint32_t sbytes = uint32_t(nr) * m.nb * 2;
+                const uint32_t mis = uint32_t(reinterpret_cast<uintptr_t>(ssrc) & 15);
+                uint8_t* sdst = sring + size_t(s) * p.sstage + mis;   // same alignment mod 16 as ssrc
+                const uint32_t head = min(sbytes, (16u - mis) & 15u);
+                const uint32_t mid = (sbytes - head) & ~15u;
+                const uint32_t tail = sbytes - head - mid;
+                for (uint32_t b = 0; b < head; ++b) sdst[b] = __ldg(ssrc + b);
+                for (uint32_t b = sbytes - tail; b < sbytes; ++b) sdst[b] = __ldg(ssrc + b);
+                if (head | tail) fence_proxy_async_smem();
+                const uint32_t fb = smem_u32(&bars[s]);
+                mbar_arrive_expect_tx(fb, qbytes + mid);
+                bulk_g2s(smem_u32(cring + size_t(s) * p.cstage), qsrc, qbytes, fb, pol);
+                if (mid) bulk_g2s(smem_u32(sdst + head), ssrc + head, mid, fb, pol);
+            }
+            if (!waited) {
+                pdl_wait();
+                pdl_launch();
+            }
+            // no copy may still be landing in shared memory when the CTA leaves
+            for (int i = (k > NST ? k - NST : 0); i < k; ++i)
+                if (!mbar_wait(smem_u32(&bars[i % NST]), (i / NST) & 1, &s_abort)) {
+                    atomicOr(&g_strata_device_error, 1 | 8);
+                    break;
+                }
+        } else {
+            pdl_wait();
+            pdl_launch();
         }
-        __syncthreads();
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumer warps
+    pdl_wait();
+    pdl_launch();
+
+    float best = -FLT_MAX;
+    int bidx = INT_MAX;
+    int tval = 0;  // head: the token of the value this lane ends up holding
+
+    StageIter<MAXM> it;
+    it.init(p, g0, g1);
+    int k = 0;  // stage counter, in step with the producer
+    while (it.valid()) {
+        const int mi = it.mi;
+        const GemvMat& m = p.m[mi];
+        const int nb = m.nb;
+        const int rows = m.rows;
+
+        // activations of this matrix -> shared memory: codes as [t][half][block] 16-byte words, and
+        // per block the T scales and dp4a seeds side by side (padded to TPP) for vector loads
+        {
+            uint4* sq = reinterpret_cast<uint4*>(xsm);
+            float* sdx = reinterpret_cast<float*>(xsm + size_t(T) * nb * 32);
+            int* sc0 = reinterpret_cast<int*>(sdx + size_t(nb) * TPP);
+            const uint4* src = reinterpret_cast<const uint4*>(m.xq);
+            for (int i = threadIdx.x; i < T * nb * 2; i += kCW * 32) {
+                const int t = i / (2 * nb);
+                const int c = i - t * 2 * nb;
+                sq[(t * 2 + (c & 1)) * nb + (c >> 1)] = __ldg(src + i);
+            }
+            for (int i = threadIdx.x; i < nb * TPP; i += kCW * 32) {
+                const int b = i / TPP, t = i - (i / TPP) * TPP;
+                float d = 0.0f;
+                int c0 = kMagicBits;
+                if (t < T) {
+                    d = __ldg(m.xd + t * nb + b);
+                    if (FMT == 0) c0 = kMagicBits - 8 * __ldg(m.xs + t * nb + b);
+                }
+                sdx[i] = d;
+                sc0[i] = c0;
+            }
+        }
+        named_bar_sync(1, kCW * 32);
+
+        const uint4* sx = reinterpret_cast<const uint4*>(xsm);
+        const float* sdx = reinterpret_cast<const float*>(xsm + size_t(T) * nb * 32);
+        const int* sc0 = reinterpret_cast<const int*>(sdx + size_t(nb) * TPP);
+        const int KS = m.ks;
+        const int NG = kCW / KS;
+        const int grp = warp / KS, wig = warp - grp * KS;
+        const int G = 32 * KS;
+        const int gl = wig * 32 + lane;
+        const int seg0 = it.sg;  // chunk j of the segment belongs to group j mod NG
+
+        for (int jj = 0; it.valid() && it.mi == mi; it.next(), ++k) {
+            const int s = k % NST;
+            const int pos = ((grp - (it.sg - seg0) % NG) + NG) % NG;  // this group's place in the stage
+            const bool active = pos < it.se - it.sg;
+            const int r0s = (it.sg - m.chunk0) * kR;   // first row of the stage
+            const int row0 = r0s + pos * kR;
+            const int nr = min(kR, rows - row0);
+            float v[V];
+#pragma unroll
+            for (int q = 0; q < V; ++q) v[q] = 0.0f;
+            const bool ok = !s_abort && mbar_wait(smem_u32(&bars[s]), (k / NST) & 1, &s_abort);
+            if (!ok) {
+                s_abort = 1;
+                atomicOr(&g_strata_device_error, 1 | 4);
+            }
+            if (ok && active) {
+                const uint8_t* cb = cring + size_t(s) * p.cstage + size_t(pos) * kR * nb * QB;
+                const uintptr_t ssrc = reinterpret_cast<uintptr_t>(m.W + size_t(rows) * nb * QB + size_t(r0s) * nb * 2);
+                const unsigned short* sc = reinterpret_cast<const unsigned short*>(
+                    sring + size_t(s) * p.sstage + (ssrc & 15) + size_t(pos) * kR * nb * 2);
+                const f32x2 negm = pack_f2(-kMagic, -kMagic);
+                f32x2 acc[kR][NP];
+#pragma unroll
+                for (int r = 0; r < kR; ++r)
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) acc[r][q] = 0ull;
+                for (int kb = gl; kb < nb; kb += G) {
+                    uint4 w[kR][QV];
+                    f32x2 dw2[kR];
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) {
+#pragma unroll
+                        for (int h = 0; h < QV; ++h)
+                            w[r][h] = *reinterpret_cast<const uint4*>(cb + (size_t(r) * nb + kb) * QB + h * 16);
+                        const float d = __half2float(__ushort_as_half(sc[r * nb + kb]));
+                        dw2[r] = pack_f2(d, d);
+                    }
+                    float dxv[TPP];
+                    int c0v[TPP];
+#pragma unroll
+                    for (int q = 0; q < TPP; q += 2) {
+                        const float2 dd = *reinterpret_cast<const float2*>(sdx + kb * TPP + q);
+                        const int2 cc = *reinterpret_cast<const int2*>(sc0 + kb * TPP + q);
+                        dxv[q] = dd.x; dxv[q + 1] = dd.y;
+                        c0v[q] = cc.x; c0v[q + 1] = cc.y;
+                    }
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) {
+                        const int ta = 2 * q, tb = 2 * q + 1;
+                        const uint4 xla = sx[(ta * 2 + 0) * nb + kb], xha = sx[(ta * 2 + 1) * nb + kb];
+                        uint4 xlb = xla, xhb = xha;
+                        if (tb < T) { xlb = sx[(tb * 2 + 0) * nb + kb]; xhb = sx[(tb * 2 + 1) * nb + kb]; }
+                        const f32x2 dx2 = pack_f2(dxv[ta], dxv[tb]);
+#pragma unroll
+                        for (int r = 0; r < kR; ++r) {
+                            int ca, cbv;
+                            if constexpr (FMT == 0) {
+                                ca = dot_q4(w[r][0], xla, xha, c0v[ta]);
+                                cbv = (tb < T) ? dot_q4(w[r][0], xlb, xhb, c0v[tb]) : kMagicBits;
+                            } else {
+                                ca = dot_q8(w[r][0], w[r][QV - 1], xla, xha, c0v[ta]);
+                                cbv = (tb < T) ? dot_q8(w[r][0], w[r][QV - 1], xlb, xhb, c0v[tb]) : kMagicBits;
+                            }
+                            // (F - 1.5*2^23) is exact; then acc += (d_w*d_x) * isum, each half one IEEE op
+                            const f32x2 f2 = add_f2(pack_f2(__int_as_float(ca), __int_as_float(cbv)), negm);
+                            acc[r][q] = fma_f2(mul_f2(dw2[r], dx2), f2, acc[r][q]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kR; ++r)
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) {
+                        float lo, hi2;
+                        unpack_f2(acc[r][q], lo, hi2);
+                        if (2 * q < T) v[r * T + 2 * q] = lo;
+                        if (2 * q + 1 < T) v[r * T + 2 * q + 1] = hi2;
+                    }
+            }
+            if (active) {
+                int vidx;
+                float tot = butterfly<V>(v, lane, vidx);
+                const bool owner = (lane & (32 / V - 1)) == 0 && vidx < kR * T;
+                const int r = vidx / T, t = vidx - (vidx / T) * T;
+                bool final_lane = (KS == 1);
+                if (KS > 1) {
+                    float* rb = red + ((jj & 1) * kCW + warp) * 32;
+                    if (owner) rb[vidx] = tot;
+                    named_bar_sync(2 + grp, G);
+                    if (wig == 0) {
+                        final_lane = true;
+                        if (owner) {
+                            const float* base = red + ((jj & 1) * kCW + grp * KS) * 32;
+                            tot = base[vidx];
+                            for (int w2 = 1; w2 < KS; ++w2) tot = __fadd_rn(tot, base[w2 * 32 + vidx]);
+                        }
+                    }
+                } else {
+                    __syncwarp();
+                }
+                if (final_lane && owner && ok && r < nr) {
+                    const int row = row0 + r;
+                    if (m.y != nullptr) m.y[size_t(t) * rows + row] = tot;
+                    if constexpr (HEAD) {
+                        tval = t;
+                        if (better(tot, row, best, bidx)) { best = tot; bidx = row; }
+                    }
+                }
+                ++jj;
+            }
+            // Every consumer warp releases every stage itself, after its own wait on that stage (and
+            // its reads): the stage can then not be refilled while any warp has yet to wait on it, so
+            // no warp can fall a full ring lap behind and mistake a later phase for this one.
+            if (lane == 0 && ok) mbar_arrive(smem_u32(&bars[NST + s]));
+        }
+        named_bar_sync(1, kCW * 32);  // everyone is done with this matrix's activations
+    }
+
+    if constexpr (HEAD) {
+        hv[threadIdx.x] = best;
+        hi[threadIdx.x] = (bidx == INT_MAX) ? INT_MAX : (bidx | (tval << 27));  // token in the top bits
+        named_bar_sync(1, kCW * 32);
         if (threadIdx.x < T) {
             const int t = threadIdx.x;
-            float bv = rv[t];
-            int bi = ri[t];
-            for (int w2 = 1; w2 < kWarps; ++w2) {
-                if (better(rv[w2 * T + t], ri[w2 * T + t], bv, bi)) { bv = rv[w2 * T + t]; bi = ri[w2 * T + t]; }
+            float bv = -FLT_MAX;
+            int bi = INT_MAX;
+            for (int q = 0; q < kCW * 32; ++q) {
+                const int code = hi[q];
+                if (code == INT_MAX || (code >> 27) != t) continue;
+                const int id = code & ((1 << 27) - 1);
+                if (better(hv[q], id, bv, bi)) { bv = hv[q]; bi = id; }
             }
-            a.cand_val[size_t(t) * gridDim.x + blockIdx.x] = bv;
-            a.cand_idx[size_t(t) * gridDim.x + blockIdx.x] = bi;
+            p.cand_val[size_t(t) * gridDim.x + blockIdx.x] = bv;
+            p.cand_idx[size_t(t) * gridDim.x + blockIdx.x] = bi;
         }
     }
 }
@@ -272,110 +507,223 @@ int device_sm_count()
     return cache[dev];
 }
 
-static size_t staged_bytes(int T, int nb, bool head)
+static int qbytes_of(int fmt) { return fmt == 0 ? 16 : 32; }
+
+// Warps per row: a function of (cols, fmt) only, so every launch of a shape (any T, single or
+// grouped) sums each row in the same order. One warp per row unless the eight groups' double-buffered
+// four-row chunks would pass ~150 KB; never more lanes than blocks.
+int gemv_warps_per_row(int64_t cols, int fmt)
 {
-    return size_t(T) * nb * 40 + (head ? size_t(kWarps) * T * 8 : 0);
+    const int64_t nb = cols / kQK;
+    const int64_t row_bytes = nb * (qbytes_of(fmt) + 2);
+    int ks = 1;
+    while (ks < kCW && int64_t(kCW / ks) * kR * row_bytes * 2 > (int64_t(150) << 10)) ks *= 2;
+    while (ks > 1 && int64_t(32) * ks > nb) ks /= 2;
+    return ks;
 }
 
-// rows a warp holds at once: only a throughput choice (it never changes any row's arithmetic)
-static int choose_R(int64_t rows, int nsm)
+// Chunks per ring stage: a power of two dividing the group count, about 32 KB of weights.
+static int stage_chunks(int64_t cols, int fmt, int ks)
 {
-    if (rows >= int64_t(4) * kWarps * 2 * nsm) return 4;
-    if (rows >= int64_t(2) * kWarps * 2 * nsm) return 2;
-    return 1;
+    const int64_t chunk = int64_t(kR) * (cols / kQK) * (qbytes_of(fmt) + 2);
+    int sg = 1;
+    while (sg * 2 <= kCW / ks && chunk * sg * 2 <= (int64_t(36) << 10)) sg *= 2;
+    return sg;
 }
 
-template <int FMT, int T, int R, bool HEAD>
-static cudaError_t launch_t(const MmvqArgs& base, int64_t rows, int nb, cudaStream_t stream, int* grid_out)
+struct Plan {
+    int cstage, sstage, ns, nb_max;
+    size_t smem;
+};
+
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kRingBudget = 176 << 10;
+constexpr int kPrefetchStages = 4;
+
+// Shared-memory plan: activation copy + fixed scratch + a ring of stages (sizes: the largest over
+// the launch's matrices), as many stages as fit in kRingBudget and shared memory (at least one).
+static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
 {
-    MmvqArgs a = base;
-    const int nsm = device_sm_count();
-    a.rg_total = int((rows + R - 1) / R);
-    const int want = (a.rg_total + kWarps - 1) / kWarps;
-    const int grid = want < nsm * 4 ? want : nsm * 4;
-    constexpr int QB = FmtInfo<FMT>::kQB;
-    const size_t rg_bytes = size_t(R) * nb * (QB + 2);
-    const size_t pf = (size_t(64) << 10) / (rg_bytes ? rg_bytes : 1);
-    a.pf_rg = int(pf < 1 ? 1 : (pf > 4096 ? 4096 : pf));
-    if (grid_out) *grid_out = grid;
-    if (HEAD && a.cand_val == nullptr) return cudaSuccess;  // size query only
-    const size_t smem = staged_bytes(T, nb, HEAD);
-    auto kern = mmvq_kernel<FMT, T, R, HEAD>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
+    Plan pl;
+    size_t cmax = 0, smax = 0;
+    int nb_max = 0;
+    for (int i = 0; i < n; ++i) {
+        const size_t rows = size_t(ms[i].sg) * kR;
+        cmax = std::max(cmax, rows * ms[i].nb * qbytes_of(fmt));
+        smax = std::max(smax, rows * ms[i].nb * 2);
+        nb_max = std::max(nb_max, ms[i].nb);
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, a);
+    pl.nb_max = nb_max;
+    pl.cstage = int((cmax + 127) & ~size_t(127));
+    pl.sstage = int((smax + 32 + 127) & ~size_t(127));
+    const int tpp = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
+    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * (T * 32 + tpp * 8) + size_t(2 * kCW * 32) * 4 +
+                         size_t(kCW * 32) * 8;
+    const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
+    const size_t per = size_t(pl.cstage) + pl.sstage;
+    const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
+    const int ns = int(std::min(kRingBudget, room) / per);
+    pl.ns = std::min(ns, 32);
+    pl.smem = base + size_t(std::max(pl.ns, 0)) * per;
+    return pl;
+}
+
+bool gemv_shape_fits(int64_t cols, int fmt, int T)
+{
+    GemvMat m = {};
+    m.nb = int(cols / kQK);
+    m.ks = gemv_warps_per_row(cols, fmt);
+    m.sg = stage_chunks(cols, fmt, m.ks);
+    const Plan pl = plan_for(T, &m, 1, fmt);
+    return pl.ns >= 1 && pl.smem <= kSmemLimit;
+}
+
+template <int FMT, int T, int MAXM, bool HEAD>
+static cudaError_t launch_gemv(GemvParams<MAXM>& prm, const Plan& pl, int grid, cudaStream_t stream)
+{
+    prm.cstage = pl.cstage;
+    prm.sstage = pl.sstage;
+    prm.ns = pl.ns;
+    prm.nb_max = pl.nb_max;
+    prm.pf = kPrefetchStages;
+    auto kern = gemv_kernel<FMT, T, MAXM, HEAD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), pl.smem, stream, prm);
+}
+
+static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq, const float* xd,
+                        const int32_t* xs, float* y, int chunk0)
+{
+    GemvMat m;
+    m.W = static_cast<const uint8_t*>(W);
+    m.xq = xq;
+    m.xd = xd;
+    m.xs = xs;
+    m.y = y;
+    m.rows = int(rows);
+    m.nb = int(cols / kQK);
+    m.ks = gemv_warps_per_row(cols, fmt);
+    m.sg = stage_chunks(cols, fmt, m.ks);
+    m.chunk0 = chunk0;
+    return m;
 }
 
 template <int FMT, int T, bool HEAD>
-static cudaError_t launch_r(const MmvqArgs& a, int64_t rows, int nb, cudaStream_t stream, int* grid_out)
+static cudaError_t single_t(const GemvMat& m, float* cv, int* ci, cudaStream_t stream, int* grid_out)
 {
-    if constexpr (HEAD) {
-        return launch_t<FMT, T, 4, true>(a, rows, nb, stream, grid_out);
-    } else {
-        switch (choose_R(rows, device_sm_count())) {
-            case 4: return launch_t<FMT, T, 4, false>(a, rows, nb, stream, grid_out);
-            case 2: return launch_t<FMT, T, 2, false>(a, rows, nb, stream, grid_out);
-            default: return launch_t<FMT, T, 1, false>(a, rows, nb, stream, grid_out);
-        }
-    }
+    GemvParams<1> prm = {};
+    prm.n_mat = 1;
+    prm.n_chunk = (m.rows + kR - 1) / kR;
+    prm.m[0] = m;
+    prm.cand_val = cv;
+    prm.cand_idx = ci;
+    const int grid = std::min(prm.n_chunk, kCtasPerSm * device_sm_count());
+    if (grid_out) *grid_out = grid;
+    if (HEAD && cv == nullptr) return cudaSuccess;  // size query
+    const Plan pl = plan_for(T, &m, 1, FMT);
+    if (pl.ns < 1) return cudaErrorInvalidValue;
+    return launch_gemv<FMT, T, 1, HEAD>(prm, pl, grid, stream);
 }
 
 template <int FMT, bool HEAD>
-static cudaError_t launch_f(const MmvqArgs& a, int64_t rows, int nb, int T, cudaStream_t stream, int* grid_out)
+static cudaError_t single_f(const GemvMat& m, int T, float* cv, int* ci, cudaStream_t s, int* g)
 {
     switch (T) {
-        case 1: return launch_r<FMT, 1, HEAD>(a, rows, nb, stream, grid_out);
-        case 2: return launch_r<FMT, 2, HEAD>(a, rows, nb, stream, grid_out);
-        case 3: return launch_r<FMT, 3, HEAD>(a, rows, nb, stream, grid_out);
-        case 4: return launch_r<FMT, 4, HEAD>(a, rows, nb, stream, grid_out);
-        case 5: return launch_r<FMT, 5, HEAD>(a, rows, nb, stream, grid_out);
-        case 6: return launch_r<FMT, 6, HEAD>(a, rows, nb, stream, grid_out);
-        case 7: return launch_r<FMT, 7, HEAD>(a, rows, nb, stream, grid_out);
-        case 8: return launch_r<FMT, 8, HEAD>(a, rows, nb, stream, grid_out);
+        case 1: return single_t<FMT, 1, HEAD>(m, cv, ci, s, g);
+        case 2: return single_t<FMT, 2, HEAD>(m, cv, ci, s, g);
+        case 3: return single_t<FMT, 3, HEAD>(m, cv, ci, s, g);
+        case 4: return single_t<FMT, 4, HEAD>(m, cv, ci, s, g);
+        case 5: return single_t<FMT, 5, HEAD>(m, cv, ci, s, g);
+        case 6: return single_t<FMT, 6, HEAD>(m, cv, ci, s, g);
+        case 7: return single_t<FMT, 7, HEAD>(m, cv, ci, s, g);
+        case 8: return single_t<FMT, 8, HEAD>(m, cv, ci, s, g);
         default: return cudaErrorInvalidValue;
     }
 }
 
-static cudaError_t dispatch(const MmvqArgs& a, int64_t rows, int nb, int fmt, int T, bool head,
-                            cudaStream_t stream, int* grid_out)
+static cudaError_t single(const GemvMat& m, int fmt, int T, bool head, float* cv, int* ci, cudaStream_t s, int* g)
 {
-    if (fmt == 0) return head ? launch_f<0, true>(a, rows, nb, T, stream, grid_out)
-                              : launch_f<0, false>(a, rows, nb, T, stream, grid_out);
-    return head ? launch_f<1, true>(a, rows, nb, T, stream, grid_out)
-                : launch_f<1, false>(a, rows, nb, T, stream, grid_out);
+    if (fmt == 0) return head ? single_f<0, true>(m, T, cv, ci, s, g) : single_f<0, false>(m, T, cv, ci, s, g);
+    return head ? single_f<1, true>(m, T, cv, ci, s, g) : single_f<1, false>(m, T, cv, ci, s, g);
 }
 
 cudaError_t launch_mmvq(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq,
                         const float* xd, const int32_t* xs, int T, float* y, cudaStream_t stream)
 {
-    MmvqArgs a = {};
-    a.W = static_cast<const uint8_t*>(W);
-    a.rows = int(rows);
-    a.nb = int(cols / kQK);
-    a.xq = xq;
-    a.xd = xd;
-    a.xs = xs;
-    a.y = y;
-    return dispatch(a, rows, a.nb, fmt, T, false, stream, nullptr);
+    const GemvMat m = make_mat(W, rows, cols, fmt, xq, xd, xs, y, 0);
+    return single(m, fmt, T, false, nullptr, nullptr, stream, nullptr);
 }
 
-// the head grid is fixed by (vocab, device), so the workspace needs only a bound on it
-static int head_grid_bound(int64_t vocab)
+// ---- grouped launch ---------------------------------------------------------------------------------
+template <int FMT, int T>
+static cudaError_t grouped_t(const strata_gemv_desc* d, int n, cudaStream_t stream)
 {
-    const int64_t rg = (vocab + 3) / 4;
-    const int64_t want = (rg + kWarps - 1) / kWarps;
-    return int(want < 4096 ? want : 4096);
+    GemvParams<kMaxGroup> prm;
+    prm.n_mat = n;
+    prm.cand_val = nullptr;
+    prm.cand_idx = nullptr;
+    int chunks = 0;
+    std::vector<double> cum(1, 0.0);
+    for (int i = 0; i < n; ++i) {
+        prm.m[i] = make_mat(d[i].W, d[i].rows, d[i].cols, FMT, d[i].xq, d[i].xd, d[i].xs, d[i].y, chunks);
+        const int nc = int((d[i].rows + kR - 1) / kR);
+        const double cb = double(kR) * (d[i].cols / kQK) * (qbytes_of(FMT) + 2);
+        for (int c = 0; c < nc; ++c) cum.push_back(cum.back() + cb);
+        chunks += nc;
+    }
+    prm.n_chunk = chunks;
+    const int grid = std::min(std::min(chunks, kCtasPerSm * device_sm_count()), kMaxGrid);
+    // split the chunk sequence into `grid` runs of about equal bytes
+    int c = 0;
+    for (int b = 0; b <= grid; ++b) {
+        const double target = cum.back() * b / grid;
+        while (c < chunks && cum[c] < target) ++c;
+        prm.plan[b] = (b == grid) ? chunks : c;
+    }
+    const Plan pl = plan_for(T, prm.m, n, FMT);
+    if (pl.ns < 1) return cudaErrorInvalidValue;
+    return launch_gemv<FMT, T, kMaxGroup, false>(prm, pl, grid, stream);
 }
 
-// scratch bytes one head launch uses on the current device (same grid formula as launch_t for R=4)
+template <int FMT>
+static cudaError_t grouped_f(const strata_gemv_desc* d, int n, int T, cudaStream_t s)
+{
+    switch (T) {
+        case 1: return grouped_t<FMT, 1>(d, n, s);
+        case 2: return grouped_t<FMT, 2>(d, n, s);
+        case 3: return grouped_t<FMT, 3>(d, n, s);
+        case 4: return grouped_t<FMT, 4>(d, n, s);
+        case 5: return grouped_t<FMT, 5>(d, n, s);
+        case 6: return grouped_t<FMT, 6>(d, n, s);
+        case 7: return grouped_t<FMT, 7>(d, n, s);
+        case 8: return grouped_t<FMT, 8>(d, n, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T, cudaStream_t stream)
+{
+    return fmt == 0 ? grouped_f<0>(d, n, T, stream) : grouped_f<1>(d, n, T, stream);
+}
+
+// ---- head ---------------------------------------------------------------------------------------------
+static int head_grid(int64_t vocab)
+{
+    const int64_t chunks = (vocab + kR - 1) / kR;
+    return int(std::min<int64_t>(chunks, int64_t(kCtasPerSm) * device_sm_count()));
+}
+
 size_t head_launch_scratch_bytes(int64_t vocab, int T)
 {
-    const int64_t rg = (vocab + 3) / 4;
-    const int64_t want = (rg + kWarps - 1) / kWarps;
-    const int64_t cap = int64_t(device_sm_count()) * 4;
-    return size_t(want < cap ? want : cap) * size_t(T) * 8;
+    return size_t(head_grid(vocab)) * size_t(T) * 8;
+}
+
+// the head grid is at most one CTA per SM; bound it without a device for the workspace query
+static int head_grid_bound(int64_t vocab)
+{
+    const int64_t chunks = (vocab + kR - 1) / kR;
+    return int(std::min<int64_t>(chunks, kMaxGrid));
 }
 
 size_t head_workspace_bytes(int64_t vocab, int T)
@@ -387,24 +735,16 @@ cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int f
                                const float* xd, const int32_t* xs, int T, int32_t* ids, float* logits,
                                void* workspace, cudaStream_t stream)
 {
-    MmvqArgs a = {};
-    a.W = static_cast<const uint8_t*>(W);
-    a.rows = int(vocab);
-    a.nb = int(cols / kQK);
-    a.xq = xq;
-    a.xd = xd;
-    a.xs = xs;
-    a.y = logits;
-    int grid = 0;
-    cudaError_t e = dispatch(a, vocab, a.nb, fmt, T, true, stream, &grid);  // size query
-    if (e != cudaSuccess) return e;
+    const GemvMat m = make_mat(W, vocab, cols, fmt, xq, xd, xs, logits, 0);
+    const int grid = head_grid(vocab);
     if (grid > head_grid_bound(vocab)) return cudaErrorInvalidValue;
-    a.cand_val = static_cast<float*>(workspace);
-    a.cand_idx = reinterpret_cast<int*>(static_cast<char*>(workspace) + size_t(grid) * T * 4);
-    e = dispatch(a, vocab, a.nb, fmt, T, true, stream, &grid);
+    float* cv = static_cast<float*>(workspace);
+    int* ci = reinterpret_cast<int*>(static_cast<char*>(workspace) + size_t(grid) * T * 4);
+    int g2 = 0;
+    cudaError_t e = single(m, fmt, T, true, cv, ci, stream, &g2);
     if (e != cudaSuccess) return e;
-    return launch_pdl(head_finalize_kernel, dim3(1), dim3(32 * T), 0, stream,
-                      (const float*)a.cand_val, (const int*)a.cand_idx, grid, T, ids);
+    return launch_pdl(head_finalize_kernel, dim3(1), dim3(32 * T), 0, stream, (const float*)cv, (const int*)ci,
+                      grid, T, ids);
 }
 
 cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq,
@@ -417,6 +757,14 @@ cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt
     if (fmt == 0)
         return launch_pdl(block_dots_kernel<0>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
     return launch_pdl(block_dots_kernel<1>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
+}
+
+cudaError_t read_device_error(int* out, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_strata_device_error, sizeof(int));
+    if (e != cudaSuccess || !clear) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_strata_device_error, &zero, sizeof(int));
 }
 
 }  // namespace strata

@@ -23,6 +23,13 @@ STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_T", -4: "ERR_FMT", 
           -6: "ERR_EXPERT", -7: "ERR_ALIGN", -8: "ERR_WORKSPACE"}
 
 
+class GemvDesc(ctypes.Structure):
+    """strata_gemv_desc of include/strata.h."""
+    _fields_ = [("W", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("xq", ctypes.c_void_p), ("xd", ctypes.c_void_p), ("xs", ctypes.c_void_p),
+                ("y", ctypes.c_void_p)]
+
+
 class StrataError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: status {status} ({STATUS.get(status, '?')})")
@@ -52,8 +59,12 @@ def lib() -> ctypes.CDLL:
             L.strata_moe_grouped.argtypes = [P, I, I64, I64, P, I64, I, P, P, P, SZ, P, P]
             L.strata_moe_debug_views.argtypes = [I, I64, I, I64, I64, P]
             L.strata_block_dots.argtypes = [P, I64, I64, I, P, P, I, P, P]
+            L.strata_mmvq_grouped.argtypes = [P, I, I, I, P]
+            L.strata_device_error.argtypes = [P, I]
+            L.strata_head_argmax_noalloc.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P]
             for name in ("strata_quantize_act", "strata_mmvq_multi", "strata_head_argmax",
-                         "strata_moe_grouped", "strata_moe_debug_views", "strata_block_dots"):
+                         "strata_moe_grouped", "strata_moe_debug_views", "strata_block_dots",
+                         "strata_mmvq_grouped", "strata_device_error", "strata_head_argmax_noalloc"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -107,6 +118,29 @@ def mmvq_multi(W, rows: int, cols: int, fmt: int, xq, xd, xs, T: int, y=None, st
     _check(lib().strata_mmvq_multi(_ptr(W), rows, cols, fmt, _ptr(xq), _ptr(xd), _ptr(xs), T, _ptr(y),
                                    _stream(stream)), "strata_mmvq_multi")
     return y
+
+
+def gemv_descs(problems) -> ctypes.Array:
+    """A strata_gemv_desc array from (W, rows, cols, xq, xd, xs, y) tuples (tensors or ints)."""
+    arr = (GemvDesc * len(problems))()
+    for i, (W, rows, cols, xq, xd, xs, y) in enumerate(problems):
+        arr[i] = GemvDesc(_ptr(W), rows, cols, _ptr(xq), _ptr(xd), _ptr(xs), _ptr(y))
+    return arr
+
+
+def mmvq_grouped(descs, fmt: int, T: int, stream=None) -> None:
+    """Run many independent T-column GEMVs (a gemv_descs array or a list of tuples) in one launch."""
+    if not isinstance(descs, ctypes.Array):
+        descs = gemv_descs(descs)
+    _check(lib().strata_mmvq_grouped(ctypes.cast(descs, ctypes.c_void_p), len(descs), fmt, T, _stream(stream)),
+           "strata_mmvq_grouped")
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's device error word (bit 0: a bounded wait in a kernel ran out)."""
+    out = ctypes.c_int(0)
+    _check(lib().strata_device_error(ctypes.byref(out), int(clear)), "strata_device_error")
+    return out.value
 
 
 def head_argmax_workspace(vocab: int, T: int) -> int:

@@ -1,12 +1,17 @@
 """A full verify window on one GPU: every projection of every layer, then the head's argmax.
 
-One step = for each of the window's matrices (48 layers x qkv/o/up/down Q4, then the Q8 head):
-quantize that projection's T fp32 input rows, run the T-column GEMV (or the head GEMV + argmax).
-The layers are not chained (no model between them): each projection has its own seeded input,
-so the step measures what the window costs — every dense weight byte read once for T tokens.
-All work is enqueued through the C ABI on one stream and can be captured in one CUDA graph;
-consecutive kernels overlap their weight prefetch with the previous kernel's tail
-(programmatic dependent launch).
+One step reads every dense weight byte of the window once for T tokens: 48 layers x (qkv, o, up,
+down) Q4 projections, then the Q8 head GEMV with its per-token argmax. The layers are not chained
+(there is no model between them): each projection has its own seeded fp32 input. Two launch
+structures are provided:
+
+  * "grouped" (the step the benchmark times): the inputs are quantized once per input width (three
+    launches), all 192 layer GEMVs run as ONE grouped launch (strata_mmvq_grouped: the matrices
+    stream back to back, every SM busy), then the head GEMV + argmax;
+  * "chained": one quantize + one GEMV launch per projection, each kernel ordered after the one
+    before it — the launch structure a chained model would need — kept for comparison.
+
+All work is enqueued through the C ABI on one stream and can be captured in one CUDA graph.
 """
 from __future__ import annotations
 
@@ -34,69 +39,101 @@ class WindowWeights:
 class VerifyWindow:
     """Buffers and launch sequence of one T-token window over ``WindowWeights``."""
 
-    def __init__(self, weights: WindowWeights, T: int, device="cuda", key="window-x", logits=False):
-        assert 1 <= T <= strata.MAX_T
-        self.wts, self.T = weights, T
+    def __init__(self, weights: WindowWeights, T: int, device="cuda", key="window-x", logits=False,
+                 mode: str = "grouped"):
+        assert 1 <= T <= strata.MAX_T and mode in ("grouped", "chained")
+        self.wts, self.T, self.mode, self.key = weights, T, mode, key
         self.shapes = weights.shapes
-        self.cols_total = sum(c for _, _, c, _ in self.shapes)
-        # one flat fp32 input buffer (so a host->device copy of a step's inputs is one copy)
-        self.x_flat = torch.empty(T * self.cols_total, dtype=torch.float32, device=device)
-        self.x, self.xq, self.xd, self.xs, self.y = [], [], [], [], []
+        n = len(self.shapes)
+        # inputs grouped by width, so that each width is quantized by one launch
+        self.widths = sorted({c for _, _, c, _ in self.shapes})
+        members = {c: [i for i, s in enumerate(self.shapes) if s[2] == c] for c in self.widths}
+        total = sum(T * c for _, _, c, _ in self.shapes)
+        self.x_flat = torch.empty(total, dtype=torch.float32, device=device)
+        self.offset = [0] * n          # element offset of each projection's input in x_flat
+        self.gx, self.gq, self.gd, self.gs = {}, {}, {}, {}
         off = 0
+        for c in self.widths:
+            k = len(members[c])
+            self.gx[c] = self.x_flat[off: off + k * T * c].view(k * T, c)
+            self.gq[c] = torch.empty((k * T, c), dtype=torch.int8, device=device)
+            self.gd[c] = torch.empty((k * T, c // 32), dtype=torch.float32, device=device)
+            self.gs[c] = torch.empty((k * T, c // 32), dtype=torch.int32, device=device)
+            for j, i in enumerate(members[c]):
+                self.offset[i] = off + j * T * c
+            off += k * T * c
+        self.x, self.xq, self.xd, self.xs, self.y = [], [], [], [], []
         for i, (name, rows, cols, fmt) in enumerate(self.shapes):
-            xi = self.x_flat[off: off + T * cols].view(T, cols)
-            off += T * cols
-            self.x.append(xi)
-            self.xq.append(torch.empty((T, cols), dtype=torch.int8, device=device))
-            self.xd.append(torch.empty((T, cols // 32), dtype=torch.float32, device=device))
-            self.xs.append(torch.empty((T, cols // 32), dtype=torch.int32, device=device))
-            last = i == len(self.shapes) - 1
+            j = members[cols].index(i)
+            self.x.append(self.gx[cols][j * T:(j + 1) * T])
+            self.xq.append(self.gq[cols][j * T:(j + 1) * T])
+            self.xd.append(self.gd[cols][j * T:(j + 1) * T])
+            self.xs.append(self.gs[cols][j * T:(j + 1) * T])
+            last = i == n - 1
             self.y.append(torch.empty((T, rows), dtype=torch.float32, device=device)
                           if (not last or logits) else None)
         self.ids = torch.empty(T, dtype=torch.int32, device=device)
-        vocab, hid = self.shapes[-1][1], self.shapes[-1][2]
+        vocab = self.shapes[-1][1]
         self.head_ws = torch.empty(strata.head_argmax_workspace(vocab, T), dtype=torch.uint8, device=device)
-        self.key = key
+        self.descs = strata.gemv_descs([(self.wts.dev[i], r, c, self.xq[i], self.xd[i], self.xs[i], self.y[i])
+                                        for i, (_, r, c, _) in enumerate(self.shapes[:-1])])
 
+    # ---- inputs ----
     def host_inputs(self) -> np.ndarray:
-        """The seeded fp32 inputs of every projection, flattened in launch order."""
-        parts = [synth.make_activations(self.T, cols, self.key, name).reshape(-1)
-                 for name, rows, cols, fmt in self.shapes]
-        return np.concatenate(parts)
+        """The seeded fp32 inputs of every projection, laid out as ``x_flat``."""
+        out = np.empty(self.x_flat.numel(), dtype=np.float32)
+        for i, (name, rows, cols, fmt) in enumerate(self.shapes):
+            out[self.offset[i]: self.offset[i] + self.T * cols] = \
+                synth.make_activations(self.T, cols, self.key, name).reshape(-1)
+        return out
+
+    def proj_input(self, host: np.ndarray, i: int) -> np.ndarray:
+        """Projection i's [T][cols] input from a ``host_inputs`` array."""
+        cols = self.shapes[i][2]
+        return host[self.offset[i]: self.offset[i] + self.T * cols].reshape(self.T, cols)
 
     def load_inputs(self, host: np.ndarray | None = None) -> None:
         host = self.host_inputs() if host is None else host
         self.x_flat.copy_(torch.from_numpy(host))
 
+    # ---- launches ----
     def launches_per_step(self) -> int:
+        if self.mode == "grouped":
+            return len(self.widths) + 1 + 2     # quantize per width, grouped GEMV, head + finalize
         return 2 * (len(self.shapes) - 1) + 3   # quantize + GEMV per layer matrix; quantize + head + finalize
 
-    def enqueue(self, stream=None, first: int = 0, last: int | None = None) -> None:
-        """Enqueue the window's matrices [first, last) (default: all) on ``stream`` (default: torch's
-        current stream): quantize each input, then its GEMV, or the head GEMV + argmax."""
+    def enqueue(self, stream=None, part: str = "all") -> None:
+        """Enqueue one window (``part``: "all", "layers" = everything before the head, "head")."""
         n = len(self.shapes)
-        last = n if last is None else last
-        for i in range(first, last):
-            name, rows, cols, fmt = self.shapes[i]
-            strata.quantize_act(self.x[i], self.xq[i], self.xd[i], self.xs[i], stream=stream)
-            if i < n - 1:
-                strata.mmvq_multi(self.wts.dev[i], rows, cols, fmt, self.xq[i], self.xd[i], self.xs[i],
-                                  self.T, self.y[i], stream=stream)
-            else:
-                strata.head_argmax(self.wts.dev[i], rows, cols, fmt, self.xq[i], self.xd[i], self.xs[i],
-                                   self.T, self.ids, self.y[i], self.head_ws, stream=stream)
+        name, vocab, hcols, hfmt = self.shapes[-1]
+        if self.mode == "grouped":
+            if part in ("all", "layers"):
+                for c in self.widths:
+                    strata.quantize_act(self.gx[c], self.gq[c], self.gd[c], self.gs[c], stream=stream)
+                strata.mmvq_grouped(self.descs, synth.Q4, self.T, stream=stream)
+        else:
+            if part in ("all", "layers"):
+                for i in range(n - 1):
+                    _, rows, cols, fmt = self.shapes[i]
+                    strata.quantize_act(self.x[i], self.xq[i], self.xd[i], self.xs[i], stream=stream)
+                    strata.mmvq_multi(self.wts.dev[i], rows, cols, fmt, self.xq[i], self.xd[i], self.xs[i],
+                                      self.T, self.y[i], stream=stream)
+            if part in ("all", "head"):
+                strata.quantize_act(self.x[n - 1], self.xq[n - 1], self.xd[n - 1], self.xs[n - 1], stream=stream)
+        if part in ("all", "head"):
+            strata.head_argmax(self.wts.dev[n - 1], vocab, hcols, hfmt, self.xq[n - 1], self.xd[n - 1],
+                               self.xs[n - 1], self.T, self.ids, self.y[n - 1], self.head_ws, stream=stream)
 
-    def capture(self, first: int = 0, last: int | None = None) -> torch.cuda.CUDAGraph:
-        """One CUDA graph of matrices [first, last) (default: the whole step), after one eager
-        warm-up pass on a side stream."""
+    def capture(self, part: str = "all") -> torch.cuda.CUDAGraph:
+        """One CUDA graph of ``part`` of the step, after one eager warm-up pass on a side stream."""
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.enqueue(first=first, last=last)
+            self.enqueue(part=part)
         torch.cuda.current_stream().wait_stream(s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.enqueue(first=first, last=last)
+            self.enqueue(part=part)
         return g
 
     def run_host(self, graph: torch.cuda.CUDAGraph, x_host: torch.Tensor, ids_host: torch.Tensor) -> None:

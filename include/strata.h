@@ -107,13 +107,49 @@ int strata_quantize_act(const float* x, int64_t n_rows, int64_t cols,
  *   W  : weight matrix [rows][cols] in `fmt` (layout above), 16-byte aligned.
  *   xq, xd, xs : quantized activations of T rows of `cols` (xq 16-byte aligned).
  *   y  : fp32 [T][rows] (token-major, rows contiguous), 4-byte aligned.
- *   1 <= T <= 8, rows >= 1, cols % 32 == 0, 32 <= cols <= 65536.
+ *   1 <= T <= 8, rows >= 1, cols % 32 == 0, 32 <= cols <= 65536, T*cols <= 131072, and the
+ *   staged activations (T*cols*1.25 bytes) plus one four-row slot of W must fit in shared memory
+ *   (for example Q8 with cols 16384 at T = 8 does not): otherwise STRATA_ERR_SHAPE.
  *   Column t is bitwise identical for every T (see the block arithmetic above).
  *   Errors: NULL, SHAPE, T, FMT, ALIGN, CUDA.
  */
 int strata_mmvq_multi(const void* W, int64_t rows, int64_t cols, int fmt,
                       const int8_t* xq, const float* xd, const int32_t* xs, int T,
                       float* y, cudaStream_t stream);
+
+/*
+ * strata_mmvq_grouped — many independent T-column GEMVs of one format in ONE launch.
+ *   Each descriptor is one strata_mmvq_multi problem; all share `fmt` and T. Outputs are bitwise
+ *   identical to separate strata_mmvq_multi calls (each row is summed in the same order). The
+ *   launch streams all matrices back to back with every SM busy and no launch gaps, for the
+ *   independent projections of a verify window (the q/k/v and gate/up products of a layer; the
+ *   layers of a window whose inputs are all known up front).
+ *   Source: verify.hpp header comment of the Strata commit "wire multi-token kernels into Verifier
+ *   and MtpDrafter CUDA graphs" (the window's cost is the dense weights read once for T tokens),
+ *   and the pull request "sm_80 (GA100) tuning", commit message on STRATA_PF_BATCH (several
+ *   experts per launch, one persistent grid a layer).
+ *   descs : HOST array of n descriptors, read during the call (1 <= n <= 192); each field as in
+ *           strata_mmvq_multi. No y may overlap another y or any input of the launch.
+ *   Errors: NULL, SHAPE, T, FMT, ALIGN, CUDA (the first bad descriptor decides).
+ */
+typedef struct {
+    const void* W;
+    int64_t rows;
+    int64_t cols;
+    const int8_t* xq;
+    const float* xd;
+    const int32_t* xs;
+    float* y;
+} strata_gemv_desc;
+int strata_mmvq_grouped(const strata_gemv_desc* descs, int n, int fmt, int T, cudaStream_t stream);
+
+/*
+ * strata_device_error — the library's device error word, read synchronously (waits for the
+ *   device). Bit 0: a bounded wait inside a kernel ran out (a bulk copy or a pipeline slot never
+ *   completed); that kernel then skipped the rest of its work and left its outputs incomplete.
+ *   clear != 0 resets the word. Returns STRATA_OK or STRATA_ERR_CUDA.
+ */
+int strata_device_error(int* out, int clear);
 
 /*
  * strata_head_argmax — vocabulary head GEMV fused with the per-token argmax.

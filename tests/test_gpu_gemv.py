@@ -222,3 +222,42 @@ def test_head_all_equal_logits_pick_id_zero():
     xq, xd, xs = oracle.quantize_act(synth.make_activations(3, cols, "flat"))
     ids = strata.head_argmax(cu(buf), vocab, cols, synth.Q8, cu(xq), cu(xd), cu(xs), 3).cpu().numpy()
     assert list(ids) == [0, 0, 0]
+
+
+# ---- grouped launch (many independent matrices, one persistent launch) -----------------------------
+@pytest.mark.parametrize("fmt,shapes,T", [
+    (synth.Q4, [(256, 512), (33, 96), (1000, 2080), (5120, 2048), (2048, 6144), (7, 4096), (1, 32)], 3),
+    (synth.Q8, [(4096, 4096), (300, 2048), (1, 32), (77, 160)], 8),
+    (synth.Q4, [(14336, 4096), (4096, 14336)], 2),
+])
+def test_grouped_equals_separate_calls_and_oracle(fmt, shapes, T):
+    probs, ref = [], []
+    for k, (rows, cols) in enumerate(shapes):
+        w = synth.make_weights(rows, cols, fmt, "grouped", k)
+        xq, xd, xs = oracle.quantize_act(synth.make_activations(T, cols, "grouped", k, outliers=True))
+        W = cu(w.buf)
+        y = torch.full((T, rows), float("nan"), device="cuda")
+        probs.append((W, rows, cols, cu(xq), cu(xd), cu(xs), y))
+        ref.append((w, xq, xd))
+    strata.mmvq_grouped(probs, fmt, T)
+    torch.cuda.synchronize()
+    for (W, rows, cols, xq, xd, xs, y), (w, xq_h, xd_h) in zip(probs, ref):
+        y1 = strata.mmvq_multi(W, rows, cols, fmt, xq, xd, xs, T)
+        assert torch.equal(y.view(torch.int32), y1.view(torch.int32)), (rows, cols)
+        sel = np.unique(np.concatenate([np.arange(0, rows, max(1, rows // 64)), [rows - 1]]))
+        y_or, A = oracle.mmvq_rows(w.buf, rows, cols, fmt, xq_h, xd_h, sel)
+        assert_within(y.cpu().numpy()[:, sel], y_or, A, f"grouped {rows}x{cols}")
+    assert strata.device_error() == 0
+
+
+def test_grouped_rejects_bad_descriptor():
+    w = torch.zeros(synth.weight_nbytes(64, 64, synth.Q4), dtype=torch.uint8, device="cuda")
+    xq = torch.zeros((1, 64), dtype=torch.int8, device="cuda")
+    xd = torch.zeros((1, 2), dtype=torch.float32, device="cuda")
+    xs = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    y = torch.zeros((1, 64), dtype=torch.float32, device="cuda")
+    good = (w, 64, 64, xq, xd, xs, y)
+    bad = (w, 64, 48, xq, xd, xs, y)
+    with pytest.raises(strata.StrataError) as e:
+        strata.mmvq_grouped([good, bad], synth.Q4, 1)
+    assert e.value.status == -2

@@ -1,13 +1,14 @@
-"""The full verify window at its real size, in the launch configuration the benchmark times (one
-CUDA graph of quantize + GEMV per projection, then the head with its argmax), against the oracle:
-every matrix on sampled rows, the head's argmax on all tokens; graph replay bitwise equal to
-eager launches; T = 4 columns bitwise equal to T = 1."""
+"""The full verify window at its real size, in the launch configurations the benchmark times (one
+CUDA graph per window: grouped = quantize per width + one grouped GEMV launch + head; chained =
+quantize + GEMV per projection + head), against the oracle: every matrix on sampled rows, the
+head's argmax on all tokens; graph replay bitwise equal to eager launches; both launch structures
+bitwise equal to each other; T = 4 columns bitwise equal to T = 1."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from block_quantized_token_strata_gb300 import synth
+from block_quantized_token_strata_gb300 import strata, synth
 from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
 
 pytestmark = pytest.mark.gpu
@@ -21,14 +22,19 @@ def weights():
     return WindowWeights(device="cuda", host_copy=True)
 
 
-def test_full_window_t4_matches_oracle(weights):
+def _bits(t):
+    return t.view(torch.int32)
+
+
+@pytest.mark.parametrize("mode", ["grouped", "chained"])
+def test_full_window_t4_matches_oracle(weights, mode):
     T = 4
-    win = VerifyWindow(weights, T, logits=True)
+    win = VerifyWindow(weights, T, logits=True, mode=mode)
     host = win.host_inputs()
     win.load_inputs(host)
     win.enqueue()
     torch.cuda.synchronize()
-    eager_y = [y.clone() if y is not None else None for y in win.y]
+    eager_y = [y.clone() for y in win.y]
     eager_ids = win.ids.clone()
 
     g = win.capture()
@@ -36,14 +42,13 @@ def test_full_window_t4_matches_oracle(weights):
         g.replay()
     torch.cuda.synchronize()
     for a, b in zip(eager_y, win.y):
-        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert torch.equal(_bits(a), _bits(b))
     assert torch.equal(eager_ids, win.ids)
+    assert strata.device_error() == 0
 
     rng = np.random.default_rng(1)
-    off = 0
     for i, (name, rows, cols, fmt) in enumerate(weights.shapes):
-        x = host[off: off + T * cols].reshape(T, cols)
-        off += T * cols
+        x = win.proj_input(host, i)
         xq, xd, xs = oracle.quantize_act(x)
         assert np.array_equal(xq, win.xq[i].cpu().numpy())
         w = weights.host[i]
@@ -65,6 +70,21 @@ def test_full_window_t4_matches_oracle(weights):
         assert (np.abs(y - y_or) <= oracle.tolerance(A)).all(), name
 
 
+def test_grouped_launch_equals_separate_calls(weights):
+    """strata_mmvq_grouped gives every matrix bitwise the output of its own strata_mmvq_multi."""
+    wg = VerifyWindow(weights, 4, logits=True, mode="grouped")
+    wc = VerifyWindow(weights, 4, logits=True, mode="chained")
+    host = wg.host_inputs()
+    wg.load_inputs(host)
+    wc.load_inputs(host)
+    wg.enqueue()
+    wc.enqueue()
+    torch.cuda.synchronize()
+    for a, b in zip(wg.y, wc.y):
+        assert torch.equal(_bits(a), _bits(b))
+    assert torch.equal(wg.ids, wc.ids)
+
+
 def test_full_window_columns_equal_single_token(weights):
     """The whole window at T = 4 vs four T = 1 windows on the same per-token inputs."""
     w4 = VerifyWindow(weights, 4, logits=True)
@@ -74,15 +94,38 @@ def test_full_window_columns_equal_single_token(weights):
     g4.replay()
     w1 = VerifyWindow(weights, 1, logits=True)
     g1 = w1.capture()
-    cols = [c for _, _, c, _ in weights.shapes]
+    n = len(weights.shapes)
     for t in range(4):
-        parts, off = [], 0
-        for c in cols:
-            parts.append(host4[off + t * c: off + (t + 1) * c])
-            off += 4 * c
-        w1.load_inputs(np.concatenate(parts))
+        h1 = np.empty(w1.x_flat.numel(), np.float32)
+        for i, (_, _, c, _) in enumerate(weights.shapes):
+            h1[w1.offset[i]: w1.offset[i] + c] = w4.proj_input(host4, i)[t]
+        w1.load_inputs(h1)
         g1.replay()
         torch.cuda.synchronize()
-        for i in range(len(cols)):
-            assert torch.equal(w1.y[i][0].view(torch.int32), w4.y[i][t].view(torch.int32)), (t, i)
+        for i in range(n):
+            assert torch.equal(_bits(w1.y[i][0]), _bits(w4.y[i][t])), (t, i)
         assert int(w1.ids[0]) == int(w4.ids[t])
+
+
+@pytest.mark.parametrize("T", [8, 7])
+def test_full_window_replays_clean_at_high_T(weights, T):
+    """Many replays of the T = 7/8 grouped window (register-heavy, slow consumer warps): no bounded
+    wait may run out (device error word stays 0) and every output equals the per-projection
+    launches bit for bit."""
+    wg = VerifyWindow(weights, T, logits=True, mode="grouped")
+    host = wg.host_inputs()
+    wg.load_inputs(host)
+    strata.device_error(clear=True)
+    g = wg.capture()
+    for _ in range(40):
+        g.replay()
+    torch.cuda.synchronize()
+    assert strata.device_error(clear=True) == 0
+    wc = VerifyWindow(weights, T, logits=True, mode="chained")
+    wc.load_inputs(host)
+    wc.enqueue()
+    torch.cuda.synchronize()
+    assert strata.device_error(clear=True) == 0
+    for a, b in zip(wg.y, wc.y):
+        assert torch.equal(_bits(a), _bits(b))
+    assert torch.equal(wg.ids, wc.ids)
