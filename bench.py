@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", default="window", choices=["window", "mmvq", "head", "moe"],
+    ap.add_argument("--case", default="window", choices=["window", "mmvq", "head", "moe", "layers"],
                     help="window: the timed step; mmvq/head/moe: a few launches of one kernel (profiling)")
     ap.add_argument("--rows", type=int, default=2048)
     ap.add_argument("--cols", type=int, default=6144)
@@ -422,6 +422,26 @@ def run_case(args):
     build.build()
     torch.cuda.set_device(0)
     T = args.T
+    if args.case == "layers":  # the window's grouped layer launch (quantize per width + one GEMV launch)
+        from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
+        wts = WindowWeights(layers=args.layers, device="cuda")
+        win = VerifyWindow(wts, T)
+        win.load_inputs()
+        g = win.capture("layers")
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.reps
+        nbytes = wts.weight_bytes - synth.weight_nbytes(synth.HEAD_VOCAB, synth.WINDOW_HIDDEN, synth.Q8)
+        print(json.dumps({"case": "layers", "layers": args.layers, "T": T, "us": ms * 1e3,
+                          "weight_gbs": nbytes / (ms * 1e-3) / 1e9, "device_error": strata.device_error()}))
+        return
     if args.case in ("mmvq", "head"):
         rows = synth.HEAD_VOCAB if args.case == "head" else args.rows
         cols = synth.WINDOW_HIDDEN if args.case == "head" else args.cols

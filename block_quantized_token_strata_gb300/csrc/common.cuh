@@ -66,11 +66,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }"
                  :: "r"(bar), "r"(bytes) : "memory");
 }
-// One probe of phase `parity` (the hardware may suspend the thread briefly before answering).
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One probe of phase `parity`. If the phase is not complete the thread is suspended in hardware
+// (issuing nothing) until it completes or about `hint_ns` pass, whichever comes first.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 20000) {
     uint32_t ok;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
     return ok != 0;
 }
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -82,16 +83,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // after an iteration cap as a backstop, or as soon as *abort becomes non-zero. The caller then
 // flags the error and leaves without touching the data the barrier guards.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kWaitIterCap = 1u << 24;
+constexpr uint32_t kWaitIterCap = 1u << 22;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < kWaitIterCap; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 63) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-        }
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
     return false;
 }

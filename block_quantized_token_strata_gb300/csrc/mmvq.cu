@@ -35,7 +35,7 @@
 
 namespace strata {
 
-constexpr int kCW = 8;                    // consumer warps
+constexpr int kCW = 12;                   // consumer warps (13 warps x 128 registers fill each SMSP's file)
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kR = 4;                     // rows per row group (= per ring slot)
 constexpr int kMaxGroup = 192;            // matrices per grouped launch
@@ -57,7 +57,7 @@ struct GemvMat {
     const int32_t* xs;
     float* y;
     int rows, nb, ks;
-    int sg;      // chunks (row groups) per ring stage
+    int lsg;     // log2 of the chunks (row groups) per ring stage
     int chunk0;  // first chunk of this matrix in the launch's chunk sequence
 };
 
@@ -67,7 +67,7 @@ struct GemvParams {
     int n_chunk;     // row groups over all matrices
     int cstage;      // bytes per stage in the code ring (multiple of 128)
     int sstage;      // bytes per stage in the scale ring (multiple of 128, 32 bytes of slack)
-    int ns;          // stages in the ring
+    int lns;         // log2 of the stages in the ring
     int nb_max;      // widest matrix, for the activation copy
     int pf;          // stages the producer prefetches into L2 ahead of its bulk copies
     float* cand_val; // head: [T][gridDim.x] per-CTA maxima
@@ -105,14 +105,30 @@ __device__ __forceinline__ float butterfly(float (&v)[V], int lane, int& vidx) {
 }
 
 template <int N> struct Pow2Ceil { static constexpr int v = N <= 1 ? 1 : 2 * Pow2Ceil<(N + 1) / 2>::v; };
+
+// Activations in shared memory, one record per block b: the T tokens' 32 codes (16-byte low half,
+// then high half, token after token), then T scales and T dp4a seeds (each padded to TPP). The
+// record size is 16 mod 32 bytes, so lanes reading consecutive blocks hit distinct bank groups, and
+// every token's operand sits at an immediate offset from one per-block address.
+template <int T>
+struct XRec {
+    static constexpr int tpp = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
+    static constexpr int raw = T * 32 + tpp * 8;
+    static constexpr int bytes = (raw % 32 == 0) ? raw + 16 : raw;
+};
+static int xrec_bytes(int T)
+{
+    const int tpp = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
+    const int raw = T * 32 + tpp * 8;
+    return (raw % 32 == 0) ? raw + 16 : raw;
+}
 template <> struct Pow2Ceil<1> { static constexpr int v = 1; };
 
-// Walks a CTA's chunks [g0, g1) as stages: within each matrix, runs of `sg` consecutive row groups
-// (about 32 KB), so that one bulk copy moves a whole stage.
+// The matrices a CTA touches, as segments: chunks [gs, ge) of matrix mi within [g0, g1).
 template <int MAXM>
-struct StageIter {
+struct SegIter {
     const GemvParams<MAXM>* p;
-    int g1, mi, sg, se, send;  // matrix, stage start, stage end, end of the matrix's run
+    int g1, mi, gs, ge;
     __device__ void init(const GemvParams<MAXM>& prm, int g0, int gend) {
         p = &prm;
         g1 = gend;
@@ -120,41 +136,62 @@ struct StageIter {
         if constexpr (MAXM > 1) {
             while (mi + 1 < prm.n_mat && prm.m[mi + 1].chunk0 <= g0) ++mi;
         }
-        sg = g0;
+        gs = g0;
         settle();
     }
     __device__ void settle() {
-        if constexpr (MAXM > 1) {
-            while (mi + 1 < p->n_mat && p->m[mi + 1].chunk0 <= sg) ++mi;
-        }
         const int mend = (MAXM > 1 && mi + 1 < p->n_mat) ? p->m[mi + 1].chunk0 : p->n_chunk;
-        send = min(g1, mend);
-        se = min(sg + p->m[mi].sg, send);
+        ge = min(g1, mend);
     }
-    __device__ bool valid() const { return sg < g1; }
-    __device__ void next() { sg = se; if (sg < g1) settle(); }
+    __device__ bool valid() const { return gs < g1; }
+    __device__ void next() { gs = ge; ++mi; if (gs < g1) settle(); }
+};
+
+// Walks a CTA's chunks as ring stages: runs of 2^lsg row groups of one matrix (about 32 KB).
+template <int MAXM>
+struct StageIter {
+    SegIter<MAXM> seg;
+    int sg, se;  // stage chunks [sg, se)
+    __device__ void init(const GemvParams<MAXM>& prm, int g0, int gend) {
+        seg.init(prm, g0, gend);
+        sg = seg.gs;
+        settle();
+    }
+    __device__ void settle() { se = min(sg + (1 << seg.p->m[seg.mi].lsg), seg.ge); }
+    __device__ bool valid() const { return sg < seg.g1; }
+    __device__ void next() {
+        sg = se;
+        if (sg >= seg.ge) {
+            seg.next();
+            if (!seg.valid()) return;
+            sg = seg.gs;
+        }
+        settle();
+    }
 };
 
 template <int FMT, int T, int MAXM, bool HEAD>
-__global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<MAXM> p)
+__global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<MAXM> p)
 {
     constexpr int QB = FmtInfo<FMT>::kQB;
     constexpr int QV = QB / 16;
     constexpr int V = Pow2Ceil<kR * T>::v;
     constexpr int TPP = T <= 2 ? 2 : (T <= 4 ? 4 : 8);  // tokens padded for the scale vectors
     constexpr int NP = (T + 1) / 2;                      // token pairs
+    constexpr int RX = XRec<T>::bytes;                   // activation record per block
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int s_abort;
 
-    const int NST = p.ns;
+    const int NST = 1 << p.lns;  // ring stages (a power of two)
+    const int lns = p.lns;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                 // full[NST], empty[NST]
     uint8_t* xsm = smem + 2 * 8 * 32;                                    // activations
-    float* red = reinterpret_cast<float*>(xsm + size_t(p.nb_max) * (T * 32 + TPP * 8));  // [2][kCW][32]
+    float* red = reinterpret_cast<float*>(xsm + p.nb_max * RX);          // [2][kCW][32]
     float* hv = red + 2 * kCW * 32;                                      // head: [kCW*32] values
     int* hi = reinterpret_cast<int*>(hv + kCW * 32);                     // head: [kCW*32] ids
     uint8_t* cring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(hi + kCW * 32) + 127) & ~uintptr_t(127));   // codes [NST][cstage]
-    uint8_t* sring = cring + size_t(NST) * p.cstage;                              // scales [NST][sstage]
+    uint8_t* sring = cring + NST * p.cstage;                                      // scales [NST][sstage]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int g0, g1;  // this CTA's chunks
@@ -187,7 +224,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
             // L2 rather than waiting out HBM latency under load.
             auto prefetch_next = [&]() {
                 if (!pf.valid()) return;
-                const GemvMat& m = p.m[pf.mi];
+                const GemvMat& m = p.m[pf.seg.mi];
                 const int r0 = (pf.sg - m.chunk0) * kR;
                 const int nr = min((pf.se - pf.sg) * kR, m.rows - r0);
                 bulk_prefetch_l2(m.W + size_t(r0) * m.nb * QB, uint32_t(nr) * m.nb * QB);
@@ -196,25 +233,25 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
                 if (hi2 > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), uint32_t(hi2 - lo));
                 pf.next();
             };
-            for (int k = 0; k < p.pf; ++k) prefetch_next();
+            for (int q = 0; q < p.pf; ++q) prefetch_next();
             bool waited = false;
             int k = 0;
             for (; it.valid(); it.next(), ++k) {
-                const int s = k % NST;
+                const int s = k & (NST - 1);
                 if (k == NST) {  // the ring is full: from here on, order after the predecessor
                     pdl_wait();
                     pdl_launch();
                     waited = true;
                 }
                 if (k >= NST) {
-                    if (!mbar_wait(smem_u32(&bars[NST + s]), ((k / NST) - 1) & 1, &s_abort)) {
+                    if (!mbar_wait(smem_u32(&bars[NST + s]), ((k >> lns) - 1) & 1, &s_abort)) {
                         s_abort = 1;
                         atomicOr(&g_strata_device_error, 1 | 2);
                         break;
                     }
                 }
                 prefetch_next();
-                const GemvMat& m = p.m[it.mi];
+                const GemvMat& m = p.m[it.seg.mi];
                 const int r0 = (it.sg - m.chunk0) * kR;
                 const int nr = min((it.se - it.sg) * kR, m.rows - r0);
                 const uint8_t* qsrc = m.W + size_t(r0) * m.nb * QB;
@@ -222,7 +259,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
                 const uint8_t* ssrc = m.W + size_t(m.rows) * m.nb * QB + size_t(r0) * m.nb * 2;
                 const uint32_t sbytes = uint32_t(nr) * m.nb * 2;
                 const uint32_t mis = uint32_t(reinterpret_cast<uintptr_t>(ssrc) & 15);
-                uint8_t* sdst = sring + size_t(s) * p.sstage + mis;   // same alignment mod 16 as ssrc
+                uint8_t* sdst = sring + s * p.sstage + mis;   // same alignment mod 16 as ssrc
                 const uint32_t head = min(sbytes, (16u - mis) & 15u);
                 const uint32_t mid = (sbytes - head) & ~15u;
                 const uint32_t tail = sbytes - head - mid;
@@ -231,7 +268,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
                 if (head | tail) fence_proxy_async_smem();
                 const uint32_t fb = smem_u32(&bars[s]);
                 mbar_arrive_expect_tx(fb, qbytes + mid);
-                bulk_g2s(smem_u32(cring + size_t(s) * p.cstage), qsrc, qbytes, fb, pol);
+                bulk_g2s(smem_u32(cring + s * p.cstage), qsrc, qbytes, fb, pol);
                 if (mid) bulk_g2s(smem_u32(sdst + head), ssrc + head, mid, fb, pol);
             }
             if (!waited) {
@@ -240,7 +277,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
             }
             // no copy may still be landing in shared memory when the CTA leaves
             for (int i = (k > NST ? k - NST : 0); i < k; ++i)
-                if (!mbar_wait(smem_u32(&bars[i % NST]), (i / NST) & 1, &s_abort)) {
+                if (!mbar_wait(smem_u32(&bars[i & (NST - 1)]), (i >> lns) & 1, &s_abort)) {
                     atomicOr(&g_strata_device_error, 1 | 8);
                     break;
                 }
@@ -259,26 +296,24 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
     int bidx = INT_MAX;
     int tval = 0;  // head: the token of the value this lane ends up holding
 
-    StageIter<MAXM> it;
-    it.init(p, g0, g1);
-    int k = 0;  // stage counter, in step with the producer
-    while (it.valid()) {
-        const int mi = it.mi;
-        const GemvMat& m = p.m[mi];
+    SegIter<MAXM> sgi;
+    sgi.init(p, g0, g1);
+    int k0 = 0;  // ring stage of the segment's first chunk, in step with the producer
+    for (; sgi.valid(); sgi.next()) {
+        const GemvMat& m = p.m[sgi.mi];
         const int nb = m.nb;
         const int rows = m.rows;
+        const int gs = sgi.gs;
+        const int nseg = sgi.ge - gs;
+        const int lsg = m.lsg;
 
-        // activations of this matrix -> shared memory: codes as [t][half][block] 16-byte words, and
-        // per block the T scales and dp4a seeds side by side (padded to TPP) for vector loads
+        // activations of this matrix -> shared memory, one record per block (see XRec)
         {
-            uint4* sq = reinterpret_cast<uint4*>(xsm);
-            float* sdx = reinterpret_cast<float*>(xsm + size_t(T) * nb * 32);
-            int* sc0 = reinterpret_cast<int*>(sdx + size_t(nb) * TPP);
             const uint4* src = reinterpret_cast<const uint4*>(m.xq);
             for (int i = threadIdx.x; i < T * nb * 2; i += kCW * 32) {
                 const int t = i / (2 * nb);
                 const int c = i - t * 2 * nb;
-                sq[(t * 2 + (c & 1)) * nb + (c >> 1)] = __ldg(src + i);
+                *reinterpret_cast<uint4*>(xsm + (c >> 1) * RX + t * 32 + (c & 1) * 16) = __ldg(src + i);
             }
             for (int i = threadIdx.x; i < nb * TPP; i += kCW * 32) {
                 const int b = i / TPP, t = i - (i / TPP) * TPP;
@@ -288,102 +323,114 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
                     d = __ldg(m.xd + t * nb + b);
                     if (FMT == 0) c0 = kMagicBits - 8 * __ldg(m.xs + t * nb + b);
                 }
-                sdx[i] = d;
-                sc0[i] = c0;
+                *reinterpret_cast<float*>(xsm + b * RX + T * 32 + t * 4) = d;
+                *reinterpret_cast<int*>(xsm + b * RX + T * 32 + TPP * 4 + t * 4) = c0;
             }
         }
         named_bar_sync(1, kCW * 32);
 
-        const uint4* sx = reinterpret_cast<const uint4*>(xsm);
-        const float* sdx = reinterpret_cast<const float*>(xsm + size_t(T) * nb * 32);
-        const int* sc0 = reinterpret_cast<const int*>(sdx + size_t(nb) * TPP);
         const int KS = m.ks;
         const int NG = kCW / KS;
         const int grp = warp / KS, wig = warp - grp * KS;
         const int G = 32 * KS;
         const int gl = wig * 32 + lane;
-        const int seg0 = it.sg;  // chunk j of the segment belongs to group j mod NG
+        const int rsw = nb * QB;  // row stride of the codes in a stage
 
-        for (int jj = 0; it.valid() && it.mi == mi; it.next(), ++k) {
-            const int s = k % NST;
-            const int pos = ((grp - (it.sg - seg0) % NG) + NG) % NG;  // this group's place in the stage
-            const bool active = pos < it.se - it.sg;
-            const int r0s = (it.sg - m.chunk0) * kR;   // first row of the stage
+        // Every consumer warp waits on, and then releases, every stage in order — also the stages in
+        // which its group has no rows. A stage is therefore never refilled before each warp has seen
+        // its current phase, so no warp can fall a ring lap behind and take a later phase for an
+        // earlier one (a parity wait cannot tell them apart). Slot, phase parity and this group's
+        // place in the stage advance incrementally.
+        const int SG = 1 << lsg;
+        int s = k0 & (NST - 1), par = (k0 >> lns) & 1;
+        int base = 0;  // group of the stage's first chunk
+        for (int c0 = 0, jj = 0; c0 < nseg; c0 += SG) {
+            int pos = grp - base;
+            if (pos < 0) pos += NG;
+            const bool active = pos < min(SG, nseg - c0);
+            const int r0s = (gs + c0 - m.chunk0) * kR;           // first row of the stage
             const int row0 = r0s + pos * kR;
             const int nr = min(kR, rows - row0);
-            float v[V];
-#pragma unroll
-            for (int q = 0; q < V; ++q) v[q] = 0.0f;
-            const bool ok = !s_abort && mbar_wait(smem_u32(&bars[s]), (k / NST) & 1, &s_abort);
+            const bool ok = !s_abort && mbar_wait(smem_u32(&bars[s]), par, &s_abort);
             if (!ok) {
                 s_abort = 1;
                 atomicOr(&g_strata_device_error, 1 | 4);
             }
-            if (ok && active) {
-                const uint8_t* cb = cring + size_t(s) * p.cstage + size_t(pos) * kR * nb * QB;
-                const uintptr_t ssrc = reinterpret_cast<uintptr_t>(m.W + size_t(rows) * nb * QB + size_t(r0s) * nb * 2);
-                const unsigned short* sc = reinterpret_cast<const unsigned short*>(
-                    sring + size_t(s) * p.sstage + (ssrc & 15) + size_t(pos) * kR * nb * 2);
-                const f32x2 negm = pack_f2(-kMagic, -kMagic);
-                f32x2 acc[kR][NP];
+            if (active) {
+                float v[V];
 #pragma unroll
-                for (int r = 0; r < kR; ++r)
+                for (int q = 0; q < V; ++q) v[q] = 0.0f;
+                if (ok) {
+                    const uint8_t* cb = cring + s * p.cstage + pos * kR * rsw;
+                    const uintptr_t ssrc = reinterpret_cast<uintptr_t>(m.W + size_t(rows) * nb * QB + size_t(r0s) * nb * 2);
+                    const unsigned short* sc = reinterpret_cast<const unsigned short*>(
+                        sring + s * p.sstage + int(ssrc & 15) + pos * (kR * 2) * nb);
+                    const f32x2 negm = pack_f2(-kMagic, -kMagic);
+                    f32x2 acc[kR][NP];
 #pragma unroll
-                    for (int q = 0; q < NP; ++q) acc[r][q] = 0ull;
-                for (int kb = gl; kb < nb; kb += G) {
-                    uint4 w[kR][QV];
-                    f32x2 dw2[kR];
+                    for (int r = 0; r < kR; ++r)
 #pragma unroll
-                    for (int r = 0; r < kR; ++r) {
-#pragma unroll
-                        for (int h = 0; h < QV; ++h)
-                            w[r][h] = *reinterpret_cast<const uint4*>(cb + (size_t(r) * nb + kb) * QB + h * 16);
-                        const float d = __half2float(__ushort_as_half(sc[r * nb + kb]));
-                        dw2[r] = pack_f2(d, d);
-                    }
-                    float dxv[TPP];
-                    int c0v[TPP];
-#pragma unroll
-                    for (int q = 0; q < TPP; q += 2) {
-                        const float2 dd = *reinterpret_cast<const float2*>(sdx + kb * TPP + q);
-                        const int2 cc = *reinterpret_cast<const int2*>(sc0 + kb * TPP + q);
-                        dxv[q] = dd.x; dxv[q + 1] = dd.y;
-                        c0v[q] = cc.x; c0v[q + 1] = cc.y;
-                    }
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        const int ta = 2 * q, tb = 2 * q + 1;
-                        const uint4 xla = sx[(ta * 2 + 0) * nb + kb], xha = sx[(ta * 2 + 1) * nb + kb];
-                        uint4 xlb = xla, xhb = xha;
-                        if (tb < T) { xlb = sx[(tb * 2 + 0) * nb + kb]; xhb = sx[(tb * 2 + 1) * nb + kb]; }
-                        const f32x2 dx2 = pack_f2(dxv[ta], dxv[tb]);
+                        for (int q = 0; q < NP; ++q) acc[r][q] = 0ull;
+                    for (int kb = gl; kb < nb; kb += G) {
+                        const uint8_t* wp = cb + kb * QB;
+                        const unsigned short* sp = sc + kb;
+                        const uint8_t* xr = xsm + kb * RX;
+                        uint4 w[kR][QV];
+                        f32x2 dw2[kR];
 #pragma unroll
                         for (int r = 0; r < kR; ++r) {
-                            int ca, cbv;
-                            if constexpr (FMT == 0) {
-                                ca = dot_q4(w[r][0], xla, xha, c0v[ta]);
-                                cbv = (tb < T) ? dot_q4(w[r][0], xlb, xhb, c0v[tb]) : kMagicBits;
-                            } else {
-                                ca = dot_q8(w[r][0], w[r][QV - 1], xla, xha, c0v[ta]);
-                                cbv = (tb < T) ? dot_q8(w[r][0], w[r][QV - 1], xlb, xhb, c0v[tb]) : kMagicBits;
+#pragma unroll
+                            for (int h = 0; h < QV; ++h)
+                                w[r][h] = *reinterpret_cast<const uint4*>(wp + r * rsw + h * 16);
+                            const float d = __half2float(__ushort_as_half(sp[r * nb]));
+                            dw2[r] = pack_f2(d, d);
+                        }
+                        float dxv[TPP];
+                        int c0v[TPP];
+#pragma unroll
+                        for (int q = 0; q < TPP; q += 2) {
+                            const float2 dd = *reinterpret_cast<const float2*>(xr + T * 32 + q * 4);
+                            const int2 cc = *reinterpret_cast<const int2*>(xr + T * 32 + TPP * 4 + q * 4);
+                            dxv[q] = dd.x; dxv[q + 1] = dd.y;
+                            c0v[q] = cc.x; c0v[q + 1] = cc.y;
+                        }
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) {
+                            const int ta = 2 * q, tb = 2 * q + 1;
+                            const uint4 xla = *reinterpret_cast<const uint4*>(xr + ta * 32);
+                            const uint4 xha = *reinterpret_cast<const uint4*>(xr + ta * 32 + 16);
+                            uint4 xlb = xla, xhb = xha;
+                            if (tb < T) {
+                                xlb = *reinterpret_cast<const uint4*>(xr + tb * 32);
+                                xhb = *reinterpret_cast<const uint4*>(xr + tb * 32 + 16);
                             }
-                            // (F - 1.5*2^23) is exact; then acc += (d_w*d_x) * isum, each half one IEEE op
-                            const f32x2 f2 = add_f2(pack_f2(__int_as_float(ca), __int_as_float(cbv)), negm);
-                            acc[r][q] = fma_f2(mul_f2(dw2[r], dx2), f2, acc[r][q]);
+                            const f32x2 dx2 = pack_f2(dxv[ta], dxv[tb]);
+#pragma unroll
+                            for (int r = 0; r < kR; ++r) {
+                                int ca, cbv;
+                                if constexpr (FMT == 0) {
+                                    ca = dot_q4(w[r][0], xla, xha, c0v[ta]);
+                                    cbv = (tb < T) ? dot_q4(w[r][0], xlb, xhb, c0v[tb]) : kMagicBits;
+                                } else {
+                                    ca = dot_q8(w[r][0], w[r][QV - 1], xla, xha, c0v[ta]);
+                                    cbv = (tb < T) ? dot_q8(w[r][0], w[r][QV - 1], xlb, xhb, c0v[tb]) : kMagicBits;
+                                }
+                                // (F - 1.5*2^23) is exact; then acc += (d_w*d_x)*isum, each half one IEEE op
+                                const f32x2 f2 = add_f2(pack_f2(__int_as_float(ca), __int_as_float(cbv)), negm);
+                                acc[r][q] = fma_f2(mul_f2(dw2[r], dx2), f2, acc[r][q]);
+                            }
                         }
                     }
+#pragma unroll
+                    for (int r = 0; r < kR; ++r)
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) {
+                            float lo, hi2;
+                            unpack_f2(acc[r][q], lo, hi2);
+                            if (2 * q < T) v[r * T + 2 * q] = lo;
+                            if (2 * q + 1 < T) v[r * T + 2 * q + 1] = hi2;
+                        }
                 }
-#pragma unroll
-                for (int r = 0; r < kR; ++r)
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        float lo, hi2;
-                        unpack_f2(acc[r][q], lo, hi2);
-                        if (2 * q < T) v[r * T + 2 * q] = lo;
-                        if (2 * q + 1 < T) v[r * T + 2 * q + 1] = hi2;
-                    }
-            }
-            if (active) {
                 int vidx;
                 float tot = butterfly<V>(v, lane, vidx);
                 const bool owner = (lane & (32 / V - 1)) == 0 && vidx < kR * T;
@@ -396,9 +443,9 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
                     if (wig == 0) {
                         final_lane = true;
                         if (owner) {
-                            const float* base = red + ((jj & 1) * kCW + grp * KS) * 32;
-                            tot = base[vidx];
-                            for (int w2 = 1; w2 < KS; ++w2) tot = __fadd_rn(tot, base[w2 * 32 + vidx]);
+                            const float* base2 = red + ((jj & 1) * kCW + grp * KS) * 32;
+                            tot = base2[vidx];
+                            for (int w2 = 1; w2 < KS; ++w2) tot = __fadd_rn(tot, base2[w2 * 32 + vidx]);
                         }
                     }
                 } else {
@@ -414,11 +461,13 @@ __global__ void __maxnreg__(112) gemv_kernel(const __grid_constant__ GemvParams<
                 }
                 ++jj;
             }
-            // Every consumer warp releases every stage itself, after its own wait on that stage (and
-            // its reads): the stage can then not be refilled while any warp has yet to wait on it, so
-            // no warp can fall a full ring lap behind and mistake a later phase for this one.
+            // this warp is done with the stage (the sums above read registers and `red` only)
             if (lane == 0 && ok) mbar_arrive(smem_u32(&bars[NST + s]));
+            if (++s == NST) { s = 0; par ^= 1; }
+            base += SG;
+            if (base >= NG) base -= NG;
         }
+        k0 += (nseg + (1 << lsg) - 1) >> lsg;
         named_bar_sync(1, kCW * 32);  // everyone is done with this matrix's activations
     }
 
@@ -510,25 +559,24 @@ int device_sm_count()
 static int qbytes_of(int fmt) { return fmt == 0 ? 16 : 32; }
 
 // Warps per row: a function of (cols, fmt) only, so every launch of a shape (any T, single or
-// grouped) sums each row in the same order. One warp per row unless the eight groups' double-buffered
-// four-row chunks would pass ~150 KB; never more lanes than blocks.
+// grouped) sums each row in the same order. As few warps as keep at least two blocks per lane
+// (fewer lanes per row = less reduction per block), at most four.
 int gemv_warps_per_row(int64_t cols, int fmt)
 {
+    (void)fmt;
     const int64_t nb = cols / kQK;
-    const int64_t row_bytes = nb * (qbytes_of(fmt) + 2);
     int ks = 1;
-    while (ks < kCW && int64_t(kCW / ks) * kR * row_bytes * 2 > (int64_t(150) << 10)) ks *= 2;
-    while (ks > 1 && int64_t(32) * ks > nb) ks /= 2;
+    while (ks < 4 && nb >= int64_t(64) * ks * 2) ks *= 2;
     return ks;
 }
 
-// Chunks per ring stage: a power of two dividing the group count, about 32 KB of weights.
-static int stage_chunks(int64_t cols, int fmt, int ks)
+// log2 of the chunks per ring stage: a power of two, at most the group count, about 32 KB.
+static int stage_chunks_log2(int64_t cols, int fmt, int ks)
 {
     const int64_t chunk = int64_t(kR) * (cols / kQK) * (qbytes_of(fmt) + 2);
-    int sg = 1;
-    while (sg * 2 <= kCW / ks && chunk * sg * 2 <= (int64_t(36) << 10)) sg *= 2;
-    return sg;
+    int l = 0;
+    while ((2 << l) <= kCW / ks && chunk * (2 << l) <= (int64_t(36) << 10)) ++l;
+    return l;
 }
 
 struct Plan {
@@ -548,7 +596,7 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     size_t cmax = 0, smax = 0;
     int nb_max = 0;
     for (int i = 0; i < n; ++i) {
-        const size_t rows = size_t(ms[i].sg) * kR;
+        const size_t rows = size_t(1 << ms[i].lsg) * kR;
         cmax = std::max(cmax, rows * ms[i].nb * qbytes_of(fmt));
         smax = std::max(smax, rows * ms[i].nb * 2);
         nb_max = std::max(nb_max, ms[i].nb);
@@ -556,14 +604,16 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     pl.nb_max = nb_max;
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
-    const int tpp = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
-    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * (T * 32 + tpp * 8) + size_t(2 * kCW * 32) * 4 +
+    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T) + size_t(2 * kCW * 32) * 4 +
                          size_t(kCW * 32) * 8;
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
     const size_t per = size_t(pl.cstage) + pl.sstage;
     const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
-    const int ns = int(std::min(kRingBudget, room) / per);
-    pl.ns = std::min(ns, 32);
+    int ns = int(std::min(kRingBudget, room) / per);
+    ns = std::min(ns, 32);
+    int pw = 1;
+    while (pw * 2 <= ns) pw *= 2;
+    pl.ns = ns >= 1 ? pw : 0;  // a power of two, so that slot and phase are a mask and a shift
     pl.smem = base + size_t(std::max(pl.ns, 0)) * per;
     return pl;
 }
@@ -573,7 +623,7 @@ bool gemv_shape_fits(int64_t cols, int fmt, int T)
     GemvMat m = {};
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks);
+    m.lsg = stage_chunks_log2(cols, fmt, m.ks);
     const Plan pl = plan_for(T, &m, 1, fmt);
     return pl.ns >= 1 && pl.smem <= kSmemLimit;
 }
@@ -583,7 +633,9 @@ static cudaError_t launch_gemv(GemvParams<MAXM>& prm, const Plan& pl, int grid, 
 {
     prm.cstage = pl.cstage;
     prm.sstage = pl.sstage;
-    prm.ns = pl.ns;
+    int lns = 0;
+    while ((2 << lns) <= pl.ns) ++lns;
+    prm.lns = lns;
     prm.nb_max = pl.nb_max;
     prm.pf = kPrefetchStages;
     auto kern = gemv_kernel<FMT, T, MAXM, HEAD>;
@@ -604,7 +656,7 @@ static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, cons
     m.rows = int(rows);
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks);
+    m.lsg = stage_chunks_log2(cols, fmt, m.ks);
     m.chunk0 = chunk0;
     return m;
 }
