@@ -65,6 +65,7 @@ struct MoeLayout {
     size_t xq, xd, xs;              // quantized x: int8 [n_tok][hidden], fp32/int32 [n_tok][hidden/32]
     size_t counts, offsets, pairs;  // int32 [n_expert], [n_expert+1], [n_tok*k]
     size_t hq, hd, hs;              // re-quantized hidden rows by pair position: [n_pair][inter], [n_pair][inter/32]
+    size_t mcum;                    // int32 [n_expert+1]: running count of 128-row M-tiles
     size_t total;
 };
 MoeLayout moe_workspace_layout(int n_expert, int64_t n_tok, int k, int64_t hidden, int64_t inter);
