@@ -176,4 +176,19 @@ __device__ __forceinline__ f32x2 add_f2(f32x2 a, f32x2 b) {
 // exact int -> float for the magic-seeded dot: one fp32 subtraction on the FMA pipe
 __device__ __forceinline__ float magic_to_float(int c) { return __fsub_rn(__int_as_float(c), kMagic); }
 
+
+// ---- per-thread asynchronous copies global -> shared (cp.async), completion by commit groups -----
+// 16 bytes, L2 only; src_bytes < 16 zero-fills the rest (0: nothing is read, the 16 bytes are zero)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// 4 bytes; src_bytes 0 writes zero
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's groups are still pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
 }  // namespace strata
