@@ -35,7 +35,32 @@
 
 namespace strata {
 
-constexpr int kCW = 12;                   // consumer warps (13 warps x 128 registers fill each SMSP's file)
+// Launch-plan tunables, fixed at compile time (the defaults are the values measured best on GB300):
+// stage size cap, ring budget, L2 prefetch distance, and the warps-per-row rule (at most KS_MAX
+// warps per row; KS doubles while every lane keeps at least KS_MINB/32 blocks).
+#ifndef STRATA_STAGE_KB
+#define STRATA_STAGE_KB 36
+#endif
+#ifndef STRATA_RING_KB
+#define STRATA_RING_KB 176
+#endif
+#ifndef STRATA_PF_STAGES
+#define STRATA_PF_STAGES 4
+#endif
+#ifndef STRATA_KS_MAX
+#define STRATA_KS_MAX 4
+#endif
+#ifndef STRATA_KS_MINB
+#define STRATA_KS_MINB 64
+#endif
+#ifndef STRATA_CW
+#define STRATA_CW 12
+#endif
+#ifndef STRATA_SG_POW2
+#define STRATA_SG_POW2 1
+#endif
+
+constexpr int kCW = STRATA_CW;            // consumer warps (+1 producer; at most 15: 16 warps x 128 registers fill the SM)
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kR = 4;                     // rows per row group (= per ring slot)
 constexpr int kMaxGroup = 192;            // matrices per grouped launch
@@ -57,7 +82,7 @@ struct GemvMat {
     const int32_t* xs;
     float* y;
     int rows, nb, ks;
-    int lsg;     // log2 of the chunks (row groups) per ring stage
+    int sg;      // chunks (row groups) per ring stage
     int chunk0;  // first chunk of this matrix in the launch's chunk sequence
 };
 
@@ -157,7 +182,7 @@ struct StageIter {
         sg = seg.gs;
         settle();
     }
-    __device__ void settle() { se = min(sg + (1 << seg.p->m[seg.mi].lsg), seg.ge); }
+    __device__ void settle() { se = min(sg + seg.p->m[seg.mi].sg, seg.ge); }
     __device__ bool valid() const { return sg < seg.g1; }
     __device__ void next() {
         sg = se;
@@ -305,7 +330,6 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
         const int rows = m.rows;
         const int gs = sgi.gs;
         const int nseg = sgi.ge - gs;
-        const int lsg = m.lsg;
 
         // activations of this matrix -> shared memory, one record per block (see XRec)
         {
@@ -341,13 +365,13 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
         // its current phase, so no warp can fall a ring lap behind and take a later phase for an
         // earlier one (a parity wait cannot tell them apart). Slot, phase parity and this group's
         // place in the stage advance incrementally.
-        const int SG = 1 << lsg;
+        const int SG = m.sg;
         int s = k0 & (NST - 1), par = (k0 >> lns) & 1;
         int base = 0;  // group of the stage's first chunk
         for (int c0 = 0, jj = 0; c0 < nseg; c0 += SG) {
             int pos = grp - base;
             if (pos < 0) pos += NG;
-            const bool active = pos < min(SG, nseg - c0);
+            const bool active = grp < NG && pos < min(SG, nseg - c0);  // warps past NG*KS idle
             const int r0s = (gs + c0 - m.chunk0) * kR;           // first row of the stage
             const int row0 = r0s + pos * kR;
             const int nr = min(kR, rows - row0);
@@ -467,7 +491,7 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
             base += SG;
             if (base >= NG) base -= NG;
         }
-        k0 += (nseg + (1 << lsg) - 1) >> lsg;
+        k0 += (nseg + SG - 1) / SG;
         named_bar_sync(1, kCW * 32);  // everyone is done with this matrix's activations
     }
 
@@ -566,17 +590,23 @@ int gemv_warps_per_row(int64_t cols, int fmt)
     (void)fmt;
     const int64_t nb = cols / kQK;
     int ks = 1;
-    while (ks < 4 && nb >= int64_t(64) * ks * 2) ks *= 2;
+    while (ks < STRATA_KS_MAX && nb >= int64_t(STRATA_KS_MINB) * ks * 2) ks *= 2;
     return ks;
 }
 
-// log2 of the chunks per ring stage: a power of two, at most the group count, about 32 KB.
-static int stage_chunks_log2(int64_t cols, int fmt, int ks)
+// Chunks per ring stage: at most the group count (every group gets at most one row group of a
+// stage), about STRATA_STAGE_KB of codes and scales; a power of two when STRATA_SG_POW2 is set.
+static int stage_chunks(int64_t cols, int fmt, int ks)
 {
     const int64_t chunk = int64_t(kR) * (cols / kQK) * (qbytes_of(fmt) + 2);
-    int l = 0;
-    while ((2 << l) <= kCW / ks && chunk * (2 << l) <= (int64_t(36) << 10)) ++l;
-    return l;
+    const int ng = kCW / ks;
+    if (STRATA_SG_POW2) {
+        int l = 0;
+        while ((2 << l) <= ng && chunk * (2 << l) <= (int64_t(STRATA_STAGE_KB) << 10)) ++l;
+        return 1 << l;
+    }
+    int sg = int(std::min<int64_t>(ng, (int64_t(STRATA_STAGE_KB) << 10) / chunk));
+    return std::max(sg, 1);
 }
 
 struct Plan {
@@ -585,8 +615,8 @@ struct Plan {
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kRingBudget = 176 << 10;
-constexpr int kPrefetchStages = 4;
+constexpr size_t kRingBudget = size_t(STRATA_RING_KB) << 10;
+constexpr int kPrefetchStages = STRATA_PF_STAGES;
 
 // Shared-memory plan: activation copy + fixed scratch + a ring of stages (sizes: the largest over
 // the launch's matrices), as many stages as fit in kRingBudget and shared memory (at least one).
@@ -596,7 +626,7 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     size_t cmax = 0, smax = 0;
     int nb_max = 0;
     for (int i = 0; i < n; ++i) {
-        const size_t rows = size_t(1 << ms[i].lsg) * kR;
+        const size_t rows = size_t(ms[i].sg) * kR;
         cmax = std::max(cmax, rows * ms[i].nb * qbytes_of(fmt));
         smax = std::max(smax, rows * ms[i].nb * 2);
         nb_max = std::max(nb_max, ms[i].nb);
@@ -623,7 +653,7 @@ bool gemv_shape_fits(int64_t cols, int fmt, int T)
     GemvMat m = {};
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.lsg = stage_chunks_log2(cols, fmt, m.ks);
+    m.sg = stage_chunks(cols, fmt, m.ks);
     const Plan pl = plan_for(T, &m, 1, fmt);
     return pl.ns >= 1 && pl.smem <= kSmemLimit;
 }
@@ -656,7 +686,7 @@ static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, cons
     m.rows = int(rows);
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.lsg = stage_chunks_log2(cols, fmt, m.ks);
+    m.sg = stage_chunks(cols, fmt, m.ks);
     m.chunk0 = chunk0;
     return m;
 }
