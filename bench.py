@@ -212,12 +212,33 @@ def run_reference(args, rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ---- multi-process bookkeeping (one process per GPU under torchrun; replicas, no data exchange) ----
+def dist_env():
+    """(world size, global rank, local rank) from the launcher's environment; (1, 0, 0) alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time for the timed region (all_reduce MAX); the identity for one process."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank processed ``units_per_rank`` in at most ``ms``."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ---- GPU arm -------------------------------------------------------------------------------------------
 def main():
     args = parse()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank)
         return
@@ -270,12 +291,8 @@ def main():
     e1.record()
     barrier()
     clocks = sampler.stop() if sampler else None
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms * 1e-3)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, "cuda")
+    value = job_rate(world, T, ms)
 
     # --- per-T lines (same graph structure), weight GB/s ---
     per_T = {}
@@ -364,7 +381,8 @@ def main():
     barrier()
     wall = (time.perf_counter() - t_wall) / n_e2e
     e2e_ms = a.elapsed_time(b) / n_e2e
-    e2e = {"value": world * T / (max(e2e_ms, wall * 1e3) * 1e-3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(max(e2e_ms, wall * 1e3), world, "cuda")
+    e2e = {"value": job_rate(world, T, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(T * 4)}
 
     # --- prompt-chunk MoE (grouped experts), reported beside the window ---
