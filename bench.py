@@ -42,8 +42,9 @@ def parse():
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", default="window", choices=["window", "mmvq", "head", "moe", "layers"],
-                    help="window: the timed step; mmvq/head/moe: a few launches of one kernel (profiling)")
+    ap.add_argument("--case", default="window", choices=["window", "mmvq", "head", "moe", "layers", "mma_peaks"],
+                    help="window: the timed step; mmvq/head/moe/layers: a few launches of one kernel "
+                         "(profiling); mma_peaks: cuBLAS int8 vs fp16 dense GEMM rates on this GPU")
     ap.add_argument("--rows", type=int, default=2048)
     ap.add_argument("--cols", type=int, default=6144)
     ap.add_argument("--fmt", type=int, default=0)
@@ -468,6 +469,34 @@ def run_case(args):
     build.build()
     torch.cuda.set_device(0)
     T = args.T
+    if args.case == "mma_peaks":  # why the MoE runs its exact integer dots as fp16 MMAs
+        n = 8192
+        out = {"case": "mma_peaks", "shape": f"{n}x{n}x{n}", "how": "cuBLAS via torch, best of 10, CUDA events"}
+        a8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        b8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        ah, bh = a8.to(torch.float16), b8.to(torch.float16)
+        ab, bb = a8.to(torch.bfloat16), b8.to(torch.bfloat16)
+        for name, fn in (("int8_tops", lambda: torch._int_mm(a8, b8.t())),
+                         ("fp16_tflops", lambda: torch.matmul(ah, bh.t())),
+                         ("bf16_tflops", lambda: torch.matmul(ab, bb.t()))):
+            try:
+                for _ in range(3):
+                    fn()
+                torch.cuda.synchronize()
+            except Exception as exc:  # an unsupported layout or dtype on this build: say so
+                out[name] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+                continue
+            best = 1e9
+            for _ in range(10):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                best = min(best, a.elapsed_time(b))
+            out[name] = 2.0 * n ** 3 / (best * 1e-3) / 1e12
+        print(json.dumps(out))
+        return
     if args.case == "layers":  # the window's grouped layer launch (quantize per width + one GEMV launch)
         from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
         wts = WindowWeights(layers=args.layers, device="cuda")
