@@ -444,11 +444,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int c0 = PHASE == 0 ? 32 * cg + 64 * half : 64 * cg + 32 * half;  // tile column
+                    uint32_t v[2][16];  // both 16-column loads of the half in flight, one wait
+                    tmem_ld16(tl + buf * 128 + c0, v[0]);
+                    tmem_ld16(tl + buf * 128 + c0 + 16, v[1]);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int q16 = 0; q16 < 2; ++q16) {
-                        uint32_t v[16];
-                        tmem_ld16(tl + buf * 128 + c0 + 16 * q16, v);
-                        tmem_ld_wait();
                         const float4* dw4 = reinterpret_cast<const float4*>(sl + 128 + c0 + 16 * q16);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -457,9 +458,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
                             f32x2& a1 = acc2[16 * half + 8 * q16 + 2 * q + 1];
                             // acc += (d_x * d_w) * isum, each half one IEEE op
                             a0 = fma_f2(mul_f2(dx2, pack_f2(dw.x, dw.y)),
-                                        pack_f2(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1])), a0);
+                                        pack_f2(__uint_as_float(v[q16][4 * q]), __uint_as_float(v[q16][4 * q + 1])), a0);
                             a1 = fma_f2(mul_f2(dx2, pack_f2(dw.z, dw.w)),
-                                        pack_f2(__uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])), a1);
+                                        pack_f2(__uint_as_float(v[q16][4 * q + 2]), __uint_as_float(v[q16][4 * q + 3])), a1);
                         }
                     }
                 }
