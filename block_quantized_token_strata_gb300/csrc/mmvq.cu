@@ -59,6 +59,12 @@ namespace strata {
 #ifndef STRATA_SG_POW2
 #define STRATA_SG_POW2 1
 #endif
+#ifndef STRATA_NST_POW2
+#define STRATA_NST_POW2 1
+#endif
+#ifndef STRATA_MAXNREG
+#define STRATA_MAXNREG 128
+#endif
 
 constexpr int kCW = STRATA_CW;            // consumer warps (+1 producer; at most 15: 16 warps x 128 registers fill the SM)
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
@@ -92,7 +98,7 @@ struct GemvParams {
     int n_chunk;     // row groups over all matrices
     int cstage;      // bytes per stage in the code ring (multiple of 128)
     int sstage;      // bytes per stage in the scale ring (multiple of 128, 32 bytes of slack)
-    int lns;         // log2 of the stages in the ring
+    int nst;         // stages in the ring (1..32)
     int nb_max;      // widest matrix, for the activation copy
     int pf;          // stages the producer prefetches into L2 ahead of its bulk copies
     float* cand_val; // head: [T][gridDim.x] per-CTA maxima
@@ -196,7 +202,7 @@ struct StageIter {
 };
 
 template <int FMT, int T, int MAXM, bool HEAD>
-__global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<MAXM> p)
+__global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ GemvParams<MAXM> p)
 {
     constexpr int QB = FmtInfo<FMT>::kQB;
     constexpr int QV = QB / 16;
@@ -207,8 +213,7 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int s_abort;
 
-    const int NST = 1 << p.lns;  // ring stages (a power of two)
-    const int lns = p.lns;
+    const int NST = p.nst;  // ring stages
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                 // full[NST], empty[NST]
     uint8_t* xsm = smem + 2 * 8 * 32;                                    // activations
     float* red = reinterpret_cast<float*>(xsm + p.nb_max * RX);          // [2][kCW][32]
@@ -260,16 +265,15 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
             };
             for (int q = 0; q < p.pf; ++q) prefetch_next();
             bool waited = false;
-            int k = 0;
-            for (; it.valid(); it.next(), ++k) {
-                const int s = k & (NST - 1);
+            int k = 0, s = 0, lap = 0;  // stage count, its slot and ring lap (k = lap * NST + s)
+            for (; it.valid(); it.next(), ++k, s = (s + 1 == NST) ? 0 : s + 1, lap += (s == 0)) {
                 if (k == NST) {  // the ring is full: from here on, order after the predecessor
                     pdl_wait();
                     pdl_launch();
                     waited = true;
                 }
                 if (k >= NST) {
-                    if (!mbar_wait(smem_u32(&bars[NST + s]), ((k >> lns) - 1) & 1, &s_abort)) {
+                    if (!mbar_wait(smem_u32(&bars[NST + s]), (lap - 1) & 1, &s_abort)) {
                         s_abort = 1;
                         atomicOr(&g_strata_device_error, 1 | 2);
                         break;
@@ -302,7 +306,7 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
             }
             // no copy may still be landing in shared memory when the CTA leaves
             for (int i = (k > NST ? k - NST : 0); i < k; ++i)
-                if (!mbar_wait(smem_u32(&bars[i & (NST - 1)]), (i >> lns) & 1, &s_abort)) {
+                if (!mbar_wait(smem_u32(&bars[i % NST]), (i / NST) & 1, &s_abort)) {
                     atomicOr(&g_strata_device_error, 1 | 8);
                     break;
                 }
@@ -366,7 +370,7 @@ __global__ void __maxnreg__(128) gemv_kernel(const __grid_constant__ GemvParams<
         // earlier one (a parity wait cannot tell them apart). Slot, phase parity and this group's
         // place in the stage advance incrementally.
         const int SG = m.sg;
-        int s = k0 & (NST - 1), par = (k0 >> lns) & 1;
+        int s = k0 % NST, par = (k0 / NST) & 1;
         int base = 0;  // group of the stage's first chunk
         for (int c0 = 0, jj = 0; c0 < nseg; c0 += SG) {
             int pos = grp - base;
@@ -643,7 +647,7 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     ns = std::min(ns, 32);
     int pw = 1;
     while (pw * 2 <= ns) pw *= 2;
-    pl.ns = ns >= 1 ? pw : 0;  // a power of two, so that slot and phase are a mask and a shift
+    pl.ns = ns >= 1 ? (STRATA_NST_POW2 ? pw : ns) : 0;
     pl.smem = base + size_t(std::max(pl.ns, 0)) * per;
     return pl;
 }
@@ -663,9 +667,7 @@ static cudaError_t launch_gemv(GemvParams<MAXM>& prm, const Plan& pl, int grid, 
 {
     prm.cstage = pl.cstage;
     prm.sstage = pl.sstage;
-    int lns = 0;
-    while ((2 << lns) <= pl.ns) ++lns;
-    prm.lns = lns;
+    prm.nst = pl.ns;
     prm.nb_max = pl.nb_max;
     prm.pf = kPrefetchStages;
     auto kern = gemv_kernel<FMT, T, MAXM, HEAD>;
