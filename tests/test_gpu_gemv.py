@@ -98,6 +98,31 @@ def test_mmvq_matches_oracle(fmt, rows, cols, T, outl):
     assert_within(y, y_or, A, f"{fmt} {rows}x{cols} T={T}")
 
 
+@pytest.mark.parametrize("fmt,T,cols", [(synth.Q4, 8, 16384), (synth.Q8, 4, 16384)])
+def test_mmvq_widest_staged_activations(fmt, T, cols):
+    """The largest activation copy the launch stages (T*cols = 131072 for Q4 at T = 8), ragged rows,
+    against the oracle on every row; the T = 1 columns are the same bits."""
+    rows = 257
+    assert strata.lib().strata_mmvq_multi(None, rows, cols, fmt, None, None, None, T, None, None) == -1
+    w = synth.make_weights(rows, cols, fmt, "widest")
+    W = cu(w.buf)
+    x = synth.make_activations(T, cols, "widest", outliers=True)
+    xq, xd, xs = gpu_quantize(x)
+    y = strata.mmvq_multi(W, rows, cols, fmt, xq, xd, xs, T).cpu().numpy()
+    y_or, A = oracle.mmvq(w.buf, rows, cols, fmt, xq.cpu().numpy(), xd.cpu().numpy())
+    assert_within(y, y_or, A, f"widest fmt={fmt} T={T}")
+    y1 = strata.mmvq_multi(W, rows, cols, fmt, xq[T - 1:], xd[T - 1:], xs[T - 1:], 1).cpu().numpy()
+    assert np.array_equal(y[T - 1].view(np.uint32), y1[0].view(np.uint32))
+
+
+def test_mmvq_rejects_activations_past_the_staged_maximum():
+    L = strata.lib()
+    A16 = 0x10000
+    # Q4 at T = 8 stages at most 131072 activation values; Q8 at T = 8 and 16384 columns does not fit
+    assert L.strata_mmvq_multi(A16, 256, 16416, synth.Q4, A16, A16, A16, 8, A16, None) == -2
+    assert L.strata_mmvq_multi(A16, 256, 16384, synth.Q8, A16, A16, A16, 8, A16, None) == -2
+
+
 @pytest.mark.parametrize("rows,cols", [(14336, 4096), (4096, 14336), (1000, 2080)])
 def test_columns_bitwise_equal_single_token(rows, cols):
     """Verify window FFN: each column at T in {2,3,4,8} is the T = 1 launch, bit for bit."""
