@@ -148,3 +148,34 @@ def test_moe_prompt_chunk_sampled(c5):
     out2 = c5.run(y_init=float("nan"))
     assert not np.isnan(out2["y"]).any()
     assert np.array_equal(out2["y"], out["y"])
+
+
+def test_moe_idle_experts_get_no_tiles():
+    """Experts no pair routes to (the first, the last and some between) hold no M-tile; the rest are
+    exact as usual."""
+    case = MoeCase(8, 256, 128, 120, 2, "moe-idle")
+    rng = np.random.default_rng(11)
+    used = np.array([1, 5, 6], np.int32)
+    ids = np.stack([rng.choice(used, size=2, replace=False) for _ in range(case.n_tok)]).astype(np.int32)
+    case.ids = ids
+    out = case.run(ids=ids)
+    counts, offsets, pairs, bad = oracle.moe_bucket(ids, case.n_exp)
+    assert bad == 0 and out["err"] == 0
+    assert np.array_equal(out["counts"], counts) and (counts[[0, 2, 3, 4, 7]] == 0).all()
+    assert np.array_equal(out["offsets"], offsets) and np.array_equal(out["pairs"], pairs)
+    check_rows(case, out, np.arange(case.n_tok * case.k))
+
+
+def test_moe_tile_boundaries():
+    """Experts with exactly 128, 129 and 1 pairs: a full M-tile, a full tile plus a one-row tile, and
+    a one-row tile; rows in a shuffled order."""
+    n_tok = 258
+    case = MoeCase(3, 128, 128, n_tok, 1, "moe-edges")
+    ids = np.concatenate([np.zeros(128), np.ones(129), [2]]).astype(np.int32)
+    np.random.default_rng(5).shuffle(ids)
+    ids = ids.reshape(n_tok, 1)
+    case.ids = ids
+    out = case.run(ids=ids)
+    counts, offsets, pairs, bad = oracle.moe_bucket(ids, 3)
+    assert list(out["counts"]) == [128, 129, 1] and np.array_equal(out["pairs"], pairs)
+    check_rows(case, out, np.arange(n_tok))
