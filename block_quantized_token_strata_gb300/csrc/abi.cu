@@ -114,9 +114,9 @@ size_t strata_head_argmax_workspace(int64_t vocab, int T)
     return head_workspace_bytes(vocab, T);
 }
 
-int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq, const float* xd,
-                       const int32_t* xs, int T, int32_t* ids, float* logits, void* workspace, size_t ws_bytes,
-                       cudaStream_t stream)
+static int head_call(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq, const float* xd,
+                     const int32_t* xs, int T, int32_t* ids, float* margin, float* logits, void* workspace,
+                     size_t ws_bytes, cudaStream_t stream)
 {
     if (!W || !ids) return STRATA_ERR_NULL;
     int st = check_acts(xq, xd, xs);
@@ -125,10 +125,26 @@ int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, cons
     if (st != STRATA_OK) return st;
     if (T < 1 || T > STRATA_MAX_T) return STRATA_ERR_T;
     if (int64_t(T) * cols > kMaxStagedTCols || !gemv_shape_fits(cols, fmt, T)) return STRATA_ERR_SHAPE;
-    if (!aligned(W, 16) || !aligned(ids, 4) || (logits && !aligned(logits, 4))) return STRATA_ERR_ALIGN;
+    if (!aligned(W, 16) || !aligned(ids, 4) || (logits && !aligned(logits, 4)) || (margin && !aligned(margin, 4)))
+        return STRATA_ERR_ALIGN;
     if (!workspace || ws_bytes < head_workspace_bytes(vocab, T)) return STRATA_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return STRATA_ERR_ALIGN;
-    return cuda_status(launch_head_argmax(W, vocab, cols, fmt, xq, xd, xs, T, ids, logits, workspace, stream));
+    return cuda_status(launch_head_argmax(W, vocab, cols, fmt, xq, xd, xs, T, ids, margin, logits, workspace, stream));
+}
+
+int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq, const float* xd,
+                       const int32_t* xs, int T, int32_t* ids, float* logits, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream)
+{
+    return head_call(W, vocab, cols, fmt, xq, xd, xs, T, ids, nullptr, logits, workspace, ws_bytes, stream);
+}
+
+int strata_head_argmax_margin(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq,
+                              const float* xd, const int32_t* xs, int T, int32_t* ids, float* margin,
+                              float* logits, void* workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!margin) return STRATA_ERR_NULL;
+    return head_call(W, vocab, cols, fmt, xq, xd, xs, T, ids, margin, logits, workspace, ws_bytes, stream);
 }
 
 int strata_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq, const int32_t* xs,

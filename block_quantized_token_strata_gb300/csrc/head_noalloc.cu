@@ -68,6 +68,6 @@ extern "C" int strata_head_argmax_noalloc(const void* W, int64_t vocab, int64_t 
     void* scratch = nullptr;
     const int st = scratch_address(&scratch);
     if (st != STRATA_OK) return st;
-    const cudaError_t e = launch_head_argmax(W, vocab, cols, fmt, xq, xd, xs, T, ids, logits, scratch, stream);
+    const cudaError_t e = launch_head_argmax(W, vocab, cols, fmt, xq, xd, xs, T, ids, nullptr, logits, scratch, stream);
     return e == cudaSuccess ? STRATA_OK : STRATA_ERR_CUDA;
 }

@@ -40,8 +40,8 @@ cudaError_t launch_mmvq(const void* W, int64_t rows, int64_t cols, int fmt, cons
 size_t head_workspace_bytes(int64_t vocab, int T);
 size_t head_launch_scratch_bytes(int64_t vocab, int T);  // bytes one launch uses on the current device
 cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq,
-                               const float* xd, const int32_t* xs, int T, int32_t* ids, float* logits,
-                               void* workspace, cudaStream_t stream);
+                               const float* xd, const int32_t* xs, int T, int32_t* ids, float* margin,
+                               float* logits, void* workspace, cudaStream_t stream);
 
 // many independent matrices of one format in one persistent launch
 cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T, cudaStream_t stream);

@@ -103,12 +103,27 @@ struct GemvParams {
     int pf;          // stages the producer prefetches into L2 ahead of its bulk copies
     float* cand_val; // head: [T][gridDim.x] per-CTA maxima
     int* cand_idx;   // head: [T][gridDim.x] their row ids
+    float* cand_sec; // head: [T][gridDim.x] per-CTA second-largest values (-inf if the CTA saw one row)
     int plan[MAXM > 1 ? kMaxGrid + 1 : 1];  // grouped: first chunk of each CTA (and the end)
     GemvMat m[MAXM];
 };
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
+}
+// Merge a candidate (best v at row i, its own second s) into a running (best bv at row bi, second bs):
+// the best by the tie rule, and the largest of the values left over (a repeated maximum counts twice,
+// so equal top values give second == best). bi == INT_MAX marks an empty side.
+__device__ __forceinline__ void top2_merge(float v, int i, float s, float& bv, int& bi, float& bs) {
+    if (i == INT_MAX) return;
+    if (better(v, i, bv, bi)) {
+        if (bi != INT_MAX) bs = fmaxf(bs, bv);
+        bs = fmaxf(bs, s);
+        bv = v;
+        bi = i;
+    } else {
+        bs = fmaxf(bs, v);  // v >= s, so the candidate's own second is covered
+    }
 }
 
 // V values per lane -> after the five xor levels lane l holds the full sum of value vidx(l).
@@ -219,8 +234,9 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     float* red = reinterpret_cast<float*>(xsm + p.nb_max * RX);          // [2][kCW][32]
     float* hv = red + 2 * kCW * 32;                                      // head: [kCW*32] values
     int* hi = reinterpret_cast<int*>(hv + kCW * 32);                     // head: [kCW*32] ids
+    float* hs = reinterpret_cast<float*>(hi + kCW * 32);                 // head: [kCW*32] second values
     uint8_t* cring = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(hi + kCW * 32) + 127) & ~uintptr_t(127));   // codes [NST][cstage]
+        (reinterpret_cast<uintptr_t>(hs + kCW * 32) + 127) & ~uintptr_t(127));   // codes [NST][cstage]
     uint8_t* sring = cring + NST * p.cstage;                                      // scales [NST][sstage]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -323,6 +339,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
 
     float best = -FLT_MAX;
     int bidx = INT_MAX;
+    float second = -INFINITY;  // head: the largest value this lane saw after `best` (a multiset's second)
     int tval = 0;  // head: the token of the value this lane ends up holding
 
     SegIter<MAXM> sgi;
@@ -484,7 +501,13 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                     if (m.y != nullptr) m.y[size_t(t) * rows + row] = tot;
                     if constexpr (HEAD) {
                         tval = t;
-                        if (better(tot, row, best, bidx)) { best = tot; bidx = row; }
+                        if (better(tot, row, best, bidx)) {
+                            if (bidx != INT_MAX) second = fmaxf(second, best);
+                            best = tot;
+                            bidx = row;
+                        } else {
+                            second = fmaxf(second, tot);
+                        }
                     }
                 }
                 ++jj;
@@ -502,47 +525,58 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     if constexpr (HEAD) {
         hv[threadIdx.x] = best;
         hi[threadIdx.x] = (bidx == INT_MAX) ? INT_MAX : (bidx | (tval << 27));  // token in the top bits
+        hs[threadIdx.x] = second;
         named_bar_sync(1, kCW * 32);
         if (threadIdx.x < T) {
             const int t = threadIdx.x;
-            float bv = -FLT_MAX;
+            float bv = -FLT_MAX, bs = -INFINITY;
             int bi = INT_MAX;
             for (int q = 0; q < kCW * 32; ++q) {
                 const int code = hi[q];
                 if (code == INT_MAX || (code >> 27) != t) continue;
                 const int id = code & ((1 << 27) - 1);
-                if (better(hv[q], id, bv, bi)) { bv = hv[q]; bi = id; }
+                top2_merge(hv[q], id, hs[q], bv, bi, bs);
             }
             p.cand_val[size_t(t) * gridDim.x + blockIdx.x] = bv;
             p.cand_idx[size_t(t) * gridDim.x + blockIdx.x] = bi;
+            if (p.cand_sec) p.cand_sec[size_t(t) * gridDim.x + blockIdx.x] = bs;
         }
     }
 }
 
-// one warp per token: reduce the per-CTA candidates with the tie rule (equal values -> lower id)
+// one warp per token: reduce the per-CTA candidates with the tie rule (equal values -> lower id);
+// with `margin`, also the largest of the other values: margin = top-1 value - top-2 value
+// (0 when the maximum occurs twice, +inf for a one-row head)
 __global__ void __launch_bounds__(256) head_finalize_kernel(const float* __restrict__ cand_val,
-                                                            const int* __restrict__ cand_idx, int ncand,
-                                                            int T, int32_t* __restrict__ ids)
+                                                            const int* __restrict__ cand_idx,
+                                                            const float* __restrict__ cand_sec, int ncand,
+                                                            int T, int32_t* __restrict__ ids,
+                                                            float* __restrict__ margin)
 {
     pdl_wait();
     pdl_launch();
     const int t = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
-    float bv = -FLT_MAX;
+    float bv = -FLT_MAX, bs = -INFINITY;
     int bi = INT_MAX;
     for (int i = lane; i < ncand; i += 32) {
         const float v = cand_val[size_t(t) * ncand + i];
         const int j = cand_idx[size_t(t) * ncand + i];
-        if (better(v, j, bv, bi)) { bv = v; bi = j; }
+        const float s = cand_sec ? cand_sec[size_t(t) * ncand + i] : -INFINITY;
+        top2_merge(v, j, s, bv, bi, bs);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+        top2_merge(ov, oi, os, bv, bi, bs);
     }
-    if (lane == 0) ids[t] = bi;
+    if (lane == 0) {
+        ids[t] = bi;
+        if (margin) margin[t] = __fsub_rn(bv, bs);
+    }
 }
 
 // test hook: isum[t][r][b] from the same dot_q4 / dot_q8 device code
@@ -639,7 +673,7 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
     const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T) + size_t(2 * kCW * 32) * 4 +
-                         size_t(kCW * 32) * 8;
+                         size_t(kCW * 32) * 12;
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
     const size_t per = size_t(pl.cstage) + pl.sstage;
     const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
@@ -703,6 +737,7 @@ static cudaError_t single_t(const GemvMat& m, float* cv, int* ci, cudaStream_t s
     prm.cand_val = cv;
     prm.cand_idx = ci;
     const int grid = std::min(prm.n_chunk, kCtasPerSm * device_sm_count());
+    prm.cand_sec = (HEAD && ci) ? reinterpret_cast<float*>(ci + size_t(grid) * T) : nullptr;  // [T][grid] after ids
     if (grid_out) *grid_out = grid;
     if (HEAD && cv == nullptr) return cudaSuccess;  // size query
     const Plan pl = plan_for(T, &m, 1, FMT);
@@ -747,6 +782,7 @@ static cudaError_t grouped_t(const strata_gemv_desc* d, int n, cudaStream_t stre
     prm.n_mat = n;
     prm.cand_val = nullptr;
     prm.cand_idx = nullptr;
+    prm.cand_sec = nullptr;
     int chunks = 0;
     std::vector<double> cum(1, 0.0);
     for (int i = 0; i < n; ++i) {
@@ -798,9 +834,10 @@ static int head_grid(int64_t vocab)
     return int(std::min<int64_t>(chunks, int64_t(kCtasPerSm) * device_sm_count()));
 }
 
+// per-CTA candidates: values, row ids and second values, each [T][grid]
 size_t head_launch_scratch_bytes(int64_t vocab, int T)
 {
-    return size_t(head_grid(vocab)) * size_t(T) * 8;
+    return size_t(head_grid(vocab)) * size_t(T) * 12;
 }
 
 // the head grid is at most one CTA per SM; bound it without a device for the workspace query
@@ -812,12 +849,12 @@ static int head_grid_bound(int64_t vocab)
 
 size_t head_workspace_bytes(int64_t vocab, int T)
 {
-    return size_t(head_grid_bound(vocab)) * size_t(T) * 8 + 256;
+    return size_t(head_grid_bound(vocab)) * size_t(T) * 12 + 256;
 }
 
 cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt, const int8_t* xq,
-                               const float* xd, const int32_t* xs, int T, int32_t* ids, float* logits,
-                               void* workspace, cudaStream_t stream)
+                               const float* xd, const int32_t* xs, int T, int32_t* ids, float* margin,
+                               float* logits, void* workspace, cudaStream_t stream)
 {
     const GemvMat m = make_mat(W, vocab, cols, fmt, xq, xd, xs, logits, 0);
     const int grid = head_grid(vocab);
@@ -827,8 +864,9 @@ cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int f
     int g2 = 0;
     cudaError_t e = single(m, fmt, T, true, cv, ci, stream, &g2);
     if (e != cudaSuccess) return e;
+    const float* cs = reinterpret_cast<const float*>(ci + size_t(grid) * T);
     return launch_pdl(head_finalize_kernel, dim3(1), dim3(32 * T), 0, stream, (const float*)cv, (const int*)ci,
-                      grid, T, ids);
+                      cs, grid, T, ids, margin);
 }
 
 cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq,

@@ -62,9 +62,11 @@ def lib() -> ctypes.CDLL:
             L.strata_mmvq_grouped.argtypes = [P, I, I, I, P]
             L.strata_device_error.argtypes = [P, I]
             L.strata_head_argmax_noalloc.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P]
+            L.strata_head_argmax_margin.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P, P, SZ, P]
             for name in ("strata_quantize_act", "strata_mmvq_multi", "strata_head_argmax",
                          "strata_moe_grouped", "strata_moe_debug_views", "strata_block_dots",
-                         "strata_mmvq_grouped", "strata_device_error", "strata_head_argmax_noalloc"):
+                         "strata_mmvq_grouped", "strata_device_error", "strata_head_argmax_noalloc",
+                         "strata_head_argmax_margin"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -161,6 +163,24 @@ def head_argmax(W, vocab: int, cols: int, fmt: int, xq, xd, xs, T: int, ids=None
                                     _ptr(logits), _ptr(workspace), ws_bytes, _stream(stream)),
            "strata_head_argmax")
     return ids
+
+
+def head_argmax_margin(W, vocab: int, cols: int, fmt: int, xq, xd, xs, T: int, ids=None, margin=None,
+                       logits=None, workspace=None, stream=None):
+    """(ids int32 [T], margin fp32 [T]): the argmax per token and its top-1 minus top-2 logit."""
+    dev = xq.device
+    if ids is None:
+        ids = torch.empty(T, dtype=torch.int32, device=dev)
+    if margin is None:
+        margin = torch.empty(T, dtype=torch.float32, device=dev)
+    need = head_argmax_workspace(vocab, T)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else need
+    _check(lib().strata_head_argmax_margin(_ptr(W), vocab, cols, fmt, _ptr(xq), _ptr(xd), _ptr(xs), T, _ptr(ids),
+                                           _ptr(margin), _ptr(logits), _ptr(workspace), ws_bytes, _stream(stream)),
+           "strata_head_argmax_margin")
+    return ids, margin
 
 
 def block_dots(W, rows: int, cols: int, fmt: int, xq, xs, T: int, isum=None, stream=None):

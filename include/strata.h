@@ -170,6 +170,22 @@ int strata_head_argmax(const void* W, int64_t vocab, int64_t cols, int fmt,
                        cudaStream_t stream);
 
 /*
+ * strata_head_argmax_margin — strata_head_argmax plus each token's top-2 margin.
+ *   Source: dsv41-offload worker/tp2.py, EmuComm.margin: the merged pick keeps the tie rule, and
+ *   the margin is the top value minus the larger of the remaining values (the two shards' best
+ *   runner-up), i.e. top-1 minus top-2 over the whole vocabulary. A maximum that occurs at two or
+ *   more ids gives margin 0; a one-row head gives +inf. It is the per-token confidence a batch of
+ *   independent sequences (one token each, T = batch) reads beside its ids.
+ *   margin : fp32 [T] device output, computed in fp32 as logits[ids[t]] - second[t] from the same
+ *   fp32 logits this call computes (and writes when `logits` is given).
+ *   Other arguments, workspace and errors as strata_head_argmax; margin NULL is STRATA_ERR_NULL.
+ */
+int strata_head_argmax_margin(const void* W, int64_t vocab, int64_t cols, int fmt,
+                              const int8_t* xq, const float* xd, const int32_t* xs, int T,
+                              int32_t* ids, float* margin, float* logits, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream);
+
+/*
  * strata_head_argmax_noalloc — strata_head_argmax for callers that cannot allocate device memory.
  *   The pages have no counterpart: this entry point exists for callers such as plugins inside a
  *   host application that owns all device memory, or servers that fix their memory at start-up,

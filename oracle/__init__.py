@@ -56,6 +56,7 @@ def _load():
             lib.or_mmvq.argtypes = [P, I64, I64, I, P, P, I64, P, P]
             lib.or_mmvq_rows.argtypes = [P, I64, I64, I, P, P, I64, P, I64, P, P]
             lib.or_argmax.argtypes = [P, I64, I64, P]
+            lib.or_margin.argtypes = [P, I64, I64, P]
             lib.or_moe_bucket.argtypes = [P, I64, I, I, P, P, P]
             lib.or_moe_bucket.restype = I64
             lib.or_moe_rows.argtypes = [P, P, P, I, I64, I64, P, I64, I, P, P, I64, P, P, P, P, P, P, P, P]
@@ -142,6 +143,17 @@ def argmax(v) -> np.ndarray:
     ids = np.empty(T, np.int32)
     _load().or_argmax(_p(v), T, n, _p(ids))
     return ids
+
+
+def margin(v) -> np.ndarray:
+    """Top-1 minus top-2 per row (a repeated maximum gives 0, a single value +inf), fp64 [T]."""
+    v = _c(v, np.float64)
+    if v.ndim == 1:
+        v = v[None, :]
+    T, n = v.shape
+    out = np.empty(T, np.float64)
+    _load().or_margin(_p(v), T, n, _p(out))
+    return out
 
 
 def head_argmax(W, vocab, cols, fmt, xq, xd):

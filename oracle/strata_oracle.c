@@ -170,6 +170,23 @@ void or_argmax(const double* v, int64_t T, int64_t n, int32_t* ids)
     }
 }
 
+/* top-2 margin of each of T rows of n values (dsv41-offload worker/tp2.py, EmuComm.margin): the
+ * largest value minus the largest of the values left once one occurrence of the largest is taken
+ * out; a maximum that occurs twice gives 0; a single value gives +inf. */
+void or_margin(const double* v, int64_t T, int64_t n, double* margin)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        const double* row = v + t * n;
+        int64_t best = 0;
+        for (int64_t i = 1; i < n; ++i)
+            if (row[i] > row[best]) best = i;
+        double second = -INFINITY;
+        for (int64_t i = 0; i < n; ++i)
+            if (i != best && row[i] > second) second = row[i];
+        margin[t] = row[best] - second;
+    }
+}
+
 /* ---- prompt-chunk MoE ---------------------------------------------------------------------------- */
 
 /* group the (token, slot) pairs per expert, ascending pair index p = tok*k + slot within an expert.

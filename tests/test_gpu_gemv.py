@@ -249,6 +249,82 @@ def test_head_all_equal_logits_pick_id_zero():
     assert list(ids) == [0, 0, 0]
 
 
+# ---- top-2 margin (batch-window confidence: top-1 minus top-2 logit per token) ------------------------
+def gpu_top2_margin(lg):
+    """fp32 top-1 minus top-2 of the GPU's own logits (a repeated maximum gives 0)."""
+    s = np.sort(lg, axis=1)
+    return (s[:, -1] - s[:, -2]).astype(np.float32)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_head_margin_matches_oracle(head_case, T):
+    c = head_case
+    logits = torch.empty((T, c["vocab"]), dtype=torch.float32, device="cuda")
+    ids, mg = strata.head_argmax_margin(c["W"], c["vocab"], c["cols"], synth.Q8, cu(c["xq"][:T]),
+                                        cu(c["xd"][:T]), cu(c["xs"][:T]), T, logits=logits)
+    ids, mg, lg = ids.cpu().numpy(), mg.cpu().numpy(), logits.cpu().numpy()
+    # the same ids as the plain head, and the margin from the same fp32 logits, bit for bit
+    ids_plain = strata.head_argmax(c["W"], c["vocab"], c["cols"], synth.Q8, cu(c["xq"][:T]), cu(c["xd"][:T]),
+                                   cu(c["xs"][:T]), T).cpu().numpy()
+    assert np.array_equal(ids, ids_plain)
+    assert np.array_equal(mg.view(np.uint32), gpu_top2_margin(lg).view(np.uint32))
+    # against the oracle: order statistics move by at most the largest per-logit bound, so the
+    # margin by at most twice that
+    mg_or = oracle.margin(c["logits"][:T])
+    bound = 2 * oracle.tolerance(c["A"][:T]).max(axis=1)
+    assert (np.abs(mg.astype(np.float64) - mg_or) <= bound).all()
+
+
+def test_head_margin_columns_bitwise_equal_single_token(head_case):
+    c = head_case
+    _, mg8 = strata.head_argmax_margin(c["W"], c["vocab"], c["cols"], synth.Q8, cu(c["xq"]), cu(c["xd"]),
+                                       cu(c["xs"]), 8)
+    mg8 = mg8.cpu().numpy()
+    for t in range(8):
+        _, mg1 = strata.head_argmax_margin(c["W"], c["vocab"], c["cols"], synth.Q8, cu(c["xq"][t:t + 1]),
+                                           cu(c["xd"][t:t + 1]), cu(c["xs"][t:t + 1]), 1)
+        assert mg1.cpu().numpy().view(np.uint32)[0] == mg8.view(np.uint32)[t]
+
+
+def test_head_margin_planted_tie_is_zero_and_one_row_is_inf():
+    """Two byte-identical rows, every other row at scale 0 (logit exactly 0), the tied logit made
+    positive: ids = the lower row, margin exactly 0. With the twin's scales zeroed too the margin is
+    the tied row's logit itself; a one-row head has margin +inf."""
+    vocab, cols = 4000, 256
+    lo, hi = 100, 3900
+    w = synth.make_weights(vocab, cols, synth.Q8, "mtie")
+    buf = w.buf.copy()
+    nb = w.nb
+    buf[hi * nb * 32:(hi + 1) * nb * 32] = buf[lo * nb * 32:(lo + 1) * nb * 32]
+    sc = buf[w.plane_bytes:].view(np.float16).reshape(vocab, nb)
+    keep = sc[lo].copy()
+    sc[:] = 0
+    sc[lo] = keep
+    sc[hi] = keep
+    xq, xd, xs = oracle.quantize_act(synth.make_activations(3, cols, "mtie"))
+    y, _ = oracle.mmvq_rows(buf, vocab, cols, synth.Q8, xq, xd, [lo])
+    neg = y[:, 0] < 0
+    xq[neg] = -xq[neg]
+    xs[neg] = -xs[neg]
+    lg = torch.empty((3, vocab), dtype=torch.float32, device="cuda")
+    ids, mg = strata.head_argmax_margin(cu(buf), vocab, cols, synth.Q8, cu(xq), cu(xd), cu(xs), 3, logits=lg)
+    assert list(ids.cpu().numpy()) == [lo] * 3 and (mg.cpu().numpy() == 0.0).all()
+    sc[hi] = 0                                     # the twin drops to 0: margin = the logit
+    ids, mg = strata.head_argmax_margin(cu(buf), vocab, cols, synth.Q8, cu(xq), cu(xd), cu(xs), 3, logits=lg)
+    assert list(ids.cpu().numpy()) == [lo] * 3
+    assert np.array_equal(mg.cpu().numpy(), lg.cpu().numpy()[:, lo])
+    w1 = synth.make_weights(1, cols, synth.Q8, "one")
+    ids1, mg1 = strata.head_argmax_margin(cu(w1.buf), 1, cols, synth.Q8, cu(xq), cu(xd), cu(xs), 3)
+    assert list(ids1.cpu().numpy()) == [0, 0, 0] and np.isinf(mg1.cpu().numpy()).all()
+
+
+def test_head_margin_rejects_null_margin():
+    L = strata.lib()
+    A16 = 0x10000
+    assert L.strata_head_argmax_margin(A16, 1000, 256, synth.Q8, A16, A16, A16, 2, A16, None, None, A16,
+                                       1 << 20, None) == -1
+
+
 # ---- grouped launch (many independent matrices, one persistent launch) -----------------------------
 @pytest.mark.parametrize("fmt,shapes,T", [
     (synth.Q4, [(256, 512), (33, 96), (1000, 2080), (5120, 2048), (2048, 6144), (7, 4096), (1, 32)], 3),

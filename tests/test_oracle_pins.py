@@ -8,6 +8,7 @@ Every oracle function is checked against something other than itself:
     matmul of codes this test packs itself;
   * the fp64 GEMV against a brute-force dense fp64 matmul of the dequantized operands;
   * the argmax tie rule against planted ties and numpy's first-occurrence argmax;
+  * the top-2 margin against hand-worked rows and the pages' two-shard merge rule;
   * the MoE grouping against numpy's stable sort, and the MoE rows against a dense brute force.
 Sources: Strata commit "wire multi-token kernels into Verifier and MtpDrafter CUDA graphs"
 (verify.hpp header comment: exact mode, q8_1 activations, pool layout (n_tok*k, n_embd));
@@ -268,3 +269,30 @@ def test_moe_rows_one_pair_equals_gemv(orc):
                        want_hidden=True)
     y, A = orc.mmvq(d.buf, hidden, inter, synth.Q4, out["hq"], out["hd"])
     assert np.array_equal(out["y"][0], y[0]) and np.array_equal(out["A"][0], A[0])
+
+
+def test_margin_hand_cases(orc):
+    """Top-1 minus top-2 (dsv41-offload worker/tp2.py, EmuComm.margin): worked by hand."""
+    oracle = orc
+    v = np.array([[1.0, 3.0, 2.0, -4.0],      # 3 - 2
+                  [5.0, 5.0, 1.0, 0.0],       # the maximum twice: 0
+                  [-1.0, -7.0, -2.5, -1.5],   # -1 - (-1.5)
+                  [0.0, 0.0, 0.0, 0.0]])      # all equal: 0
+    assert list(oracle.margin(v)) == [1.0, 0.0, 0.5, 0.0]
+    assert oracle.margin(np.array([[2.5]]))[0] == np.inf    # one value: nothing to beat
+
+
+def test_margin_matches_two_shard_merge(orc):
+    """The pages' two-shard merge: split each row at a random point, take each shard's top-2, merge
+    as EmuComm.margin does (take_a = a1 >= b1; second = max(a2, b1) or max(b2, a1)); equals the
+    whole-row margin. Ties are planted so that both branches and equal maxima occur."""
+    oracle = orc
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        n = int(rng.integers(4, 40))
+        row = rng.integers(-5, 6, size=n).astype(np.float64)   # small integers: many ties
+        cut = int(rng.integers(2, n - 1))
+        A, B = np.sort(row[:cut])[::-1], np.sort(row[cut:])[::-1]
+        a1, a2, b1, b2 = A[0], A[1], B[0], B[1]
+        second = max(a2, b1) if a1 >= b1 else max(b2, a1)
+        assert oracle.margin(row)[0] == max(a1, b1) - second
