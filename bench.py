@@ -345,6 +345,29 @@ def main():
                 "head": {"gbs": head_bytes / (head_ms * 1e-3) / 1e9, "us": head_ms * 1e3,
                          "frac": head_bytes / (head_ms * 1e-3) / 1e9 / hbm_peak}}
 
+    # --- batch head: 8 independent sequences at one token each, ids + top-2 margin per sequence
+    wb = wins[8]
+    hb = {"T": 8}
+    ids_b = torch.empty(8, dtype=torch.int32, device="cuda")
+    mg_b = torch.empty(8, dtype=torch.float32, device="cuda")
+    def head_margin():
+        strata.head_argmax_margin(wb.wts.dev[-1], vr, vc, vf, wb.xq[-1], wb.xd[-1], wb.xs[-1], 8, ids=ids_b,
+                                  margin=mg_b, workspace=wb.head_ws)
+    for _ in range(3):
+        head_margin()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(20):
+        head_margin()
+    b.record()
+    torch.cuda.synchronize()
+    hm_ms = a.elapsed_time(b) / 20
+    hb_bytes = synth.weight_nbytes(vr, vc, vf) + 8 * vc * 1.25
+    hb.update({"us": hm_ms * 1e3, "gbs": hb_bytes / (hm_ms * 1e-3) / 1e9,
+               "frac": hb_bytes / (hm_ms * 1e-3) / 1e9 / hbm_peak,
+               "note": "strata_head_argmax_margin on the Q8 head: ids and top-1 minus top-2 logit per sequence"})
+
     # --- the same window with one quantize + GEMV launch per projection (chained launch structure)
     wch = VerifyWindow(wts, T, mode="chained")
     wch.load_inputs()
@@ -409,7 +432,8 @@ def main():
                                 "launch over the 192 layer matrices, head GEMV + argmax"},
             "weight_gbs": wts.weight_bytes / (ms * 1e-3) / 1e9 * world,
             "hbm_frac": wts.weight_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
-            "per_T": per_T, "chained_launches": chained, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "per_T": per_T, "chained_launches": chained, "batch_head_margin": hb, "roofline": roofline,
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe,
             "device_error_word": strata.device_error(),
         }
