@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", default="window", choices=["window", "mmvq", "head", "moe", "layers", "mma_peaks"],
+    ap.add_argument("--case", default="window",
+                    choices=["window", "mmvq", "head", "moe", "layers", "mma_peaks", "gemm"],
                     help="window: the timed step; mmvq/head/moe/layers: a few launches of one kernel "
                          "(profiling); mma_peaks: cuBLAS int8 vs fp16 dense GEMM rates on this GPU")
     ap.add_argument("--rows", type=int, default=2048)
@@ -410,9 +411,10 @@ def main():
            "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(T * 4)}
 
     # --- prompt-chunk MoE (grouped experts), reported beside the window ---
-    moe = None
+    moe = gemm = None
     if not args.no_moe:
         moe = bench_moe(torch, strata, synth, args)
+        gemm = bench_prompt_gemm(torch, strata, synth)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -434,12 +436,36 @@ def main():
             "hbm_frac": wts.weight_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
             "per_T": per_T, "chained_launches": chained, "batch_head_margin": hb, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe,
+            "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe, "prompt_gemm": gemm,
             "device_error_word": strata.device_error(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def bench_prompt_gemm(torch, strata, synth, reps=20):
+    """The dense prompt GEMM: a 3,259-token chunk against the window's FFN up projection (Q4 6144 x 2048)."""
+    rows, cols, n_tok = 6144, 2048, 3259
+    W = torch.from_numpy(synth.make_weights(rows, cols, synth.Q4, "prompt-gemm").buf).cuda()
+    xq, xd, _ = strata.quantize_act(torch.from_numpy(synth.make_activations(n_tok, cols, "prompt-gemm")).cuda())
+    y = torch.empty((n_tok, rows), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        strata.gemm_q4(W, rows, cols, xq, xd, y=y)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        strata.gemm_q4(W, rows, cols, xq, xd, y=y)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    tf = 2.0 * n_tok * rows * cols / (ms * 1e-3) / 1e12
+    peak, kind = tensor_peak()
+    return {"workload": "3,259-token prompt chunk x Q4 6144x2048 (the window's FFN up projection)",
+            "ms": ms, "tokens_per_s": n_tok / (ms * 1e-3),
+            "tensor": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                       "peak_kind": kind}}
 
 
 def bench_moe(torch, strata, synth, args, reps=20):
@@ -520,6 +546,9 @@ def run_case(args):
                 best = min(best, a.elapsed_time(b))
             out[name] = 2.0 * n ** 3 / (best * 1e-3) / 1e12
         print(json.dumps(out))
+        return
+    if args.case == "gemm":  # the dense prompt GEMM
+        print(json.dumps({"case": "gemm", **bench_prompt_gemm(torch, strata, synth, reps=args.reps)}))
         return
     if args.case == "layers":  # the window's grouped layer launch (quantize per width + one GEMV launch)
         from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights

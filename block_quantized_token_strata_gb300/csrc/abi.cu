@@ -147,6 +147,16 @@ int strata_head_argmax_margin(const void* W, int64_t vocab, int64_t cols, int fm
     return head_call(W, vocab, cols, fmt, xq, xd, xs, T, ids, margin, logits, workspace, ws_bytes, stream);
 }
 
+int strata_gemm_q4(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd, int64_t n_tok,
+                   float* y, cudaStream_t stream)
+{
+    if (!W || !xq || !xd || !y) return STRATA_ERR_NULL;
+    if (rows < 128 || rows % 128 != 0 || cols < 64 || cols % 64 != 0 || n_tok < 1) return STRATA_ERR_SHAPE;
+    if (rows > 65536 || cols > 65536 || n_tok > (int64_t(1) << 24)) return STRATA_ERR_SHAPE;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(xd, 4) || !aligned(y, 16)) return STRATA_ERR_ALIGN;
+    return cuda_status(launch_prompt_gemm(W, rows, cols, xq, xd, n_tok, y, stream));
+}
+
 int strata_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq, const int32_t* xs,
                       int T, int32_t* isum, cudaStream_t stream)
 {

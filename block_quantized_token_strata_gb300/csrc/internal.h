@@ -74,5 +74,7 @@ struct ExpertPtrs;  // device-side view of strata_expert (three const void*)
 cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden, int64_t inter,
                                const int32_t* ids, int64_t n_tok, int k, const float* x, float* y,
                                uint8_t* ws, const MoeLayout& L, int32_t* err_word, cudaStream_t stream);
+cudaError_t launch_prompt_gemm(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                               int64_t n_tok, float* y, cudaStream_t stream);
 
 }  // namespace strata

@@ -159,6 +159,10 @@ struct MoeTcArgs {
     float* hd;
     int32_t* hs;
     float* y;
+    // dense prompt GEMM (down-phase kernel only): the one Q4 matrix [hidden][inter] and the number of
+    // activation rows; tiles then cover rows 0.. in order and row m of the output is y row m
+    const uint8_t* dense_w;
+    int dense_rows;
 };
 
 // byte offset of row r, 8-element column group c in a 128-row x 32-element K-major fp16 tile
@@ -178,6 +182,12 @@ __device__ __forceinline__ TcTile tc_tile(const MoeTcArgs& a, int t, int NT)
     TcTile tl;
     const int u = t / NT;
     tl.nt = t - u * NT;
+    if (a.dense_w) {
+        tl.e = 0;
+        tl.m0 = u * 128;
+        tl.mvalid = min(128, a.dense_rows - u * 128);
+        return tl;
+    }
     int lo = 0, hi = a.n_expert;  // largest e with mcum[e] <= u
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -200,7 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
     pdl_wait();  // the grouping, the tile counts and the activations come from the kernels ahead
     pdl_launch();
     const int NT = PHASE == 0 ? a.inter / 64 : a.hidden / 128;
-    const int total = a.mcum[a.n_expert] * NT;
+    const int total = (a.dense_w ? (a.dense_rows + 127) / 128 : a.mcum[a.n_expert]) * NT;
     if (int(blockIdx.x) >= total) return;
     const int KB = PHASE == 0 ? a.hidden / 32 : a.inter / 32;
 
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
         auto seek = [&]() {
             if (it >= total) return;
             const TcTile tl = tc_tile(a, it, NT);
-            const ExpertPtrs ex = a.experts[tl.e];
+            const ExpertPtrs ex = a.dense_w ? ExpertPtrs{nullptr, nullptr, a.dense_w} : a.experts[tl.e];
             const bool rvalid = r < tl.mvalid;
             const int P = tl.m0 + (rvalid ? r : 0);
             if (PHASE == 0) {
@@ -426,7 +436,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const TcTile tile = tc_tile(a, t, NT);
             // down phase: the output row of this thread's pair, loaded now, used after the K loop
-            const int prow = (PHASE == 1 && m < tile.mvalid) ? __ldg(a.pairs + tile.m0 + m) : 0;
+            const int prow = (PHASE == 1 && m < tile.mvalid)
+                                 ? (a.dense_w ? tile.m0 + m : __ldg(a.pairs + tile.m0 + m)) : 0;
             f32x2 acc2[32];  // acc2[q] = columns (2q, 2q+1) of this thread's 64
 #pragma unroll
             for (int q = 0; q < 32; ++q) acc2[q] = 0ull;
@@ -570,7 +581,7 @@ cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden
     e = launch_pdl(moe_tiles_kernel, dim3(1), dim3(32), 0, stream, (const int32_t*)counts, n_expert, mcum);
     if (e != cudaSuccess) return e;
 
-    MoeTcArgs a;
+    MoeTcArgs a = {};  // dense_w null: the grouped MoE
     a.experts = ex;
     a.n_expert = n_expert;
     a.hidden = int(hidden);
@@ -599,6 +610,28 @@ cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden
     e = launch_pdl(moe_tc_kernel<0>, dim3(unsigned(grid0)), dim3(kTcThreads), kTcSmem, stream, a);
     if (e != cudaSuccess) return e;
     return launch_pdl(moe_tc_kernel<1>, dim3(unsigned(grid1)), dim3(kTcThreads), kTcSmem, stream, a);
+}
+
+// Dense prompt GEMM y[n][r] = sum_b (d_w[r][b] * xd[n][b]) * isum[n][r][b] on the tensor cores: the
+// down-phase kernel with one matrix and the activation rows in order (no grouping).
+cudaError_t launch_prompt_gemm(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                               int64_t n_tok, float* y, cudaStream_t stream)
+{
+    MoeTcArgs a = {};
+    a.n_expert = 1;
+    a.hidden = int(rows);
+    a.inter = int(cols);
+    a.k = 1;
+    a.hq = const_cast<int8_t*>(xq);
+    a.hd = const_cast<float*>(xd);
+    a.y = y;
+    a.dense_w = static_cast<const uint8_t*>(W);
+    a.dense_rows = int(n_tok);
+    cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((n_tok + 127) / 128) * (rows / 128);
+    const int grid = int(std::min<int64_t>(tiles, device_sm_count()));
+    return launch_pdl(moe_tc_kernel<1>, dim3(unsigned(grid)), dim3(kTcThreads), kTcSmem, stream, a);
 }
 
 }  // namespace strata

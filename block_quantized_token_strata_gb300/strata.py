@@ -63,10 +63,11 @@ def lib() -> ctypes.CDLL:
             L.strata_device_error.argtypes = [P, I]
             L.strata_head_argmax_noalloc.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P]
             L.strata_head_argmax_margin.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P, P, SZ, P]
+            L.strata_gemm_q4.argtypes = [P, I64, I64, P, P, I64, P, P]
             for name in ("strata_quantize_act", "strata_mmvq_multi", "strata_head_argmax",
                          "strata_moe_grouped", "strata_moe_debug_views", "strata_block_dots",
                          "strata_mmvq_grouped", "strata_device_error", "strata_head_argmax_noalloc",
-                         "strata_head_argmax_margin"):
+                         "strata_head_argmax_margin", "strata_gemm_q4"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -181,6 +182,16 @@ def head_argmax_margin(W, vocab: int, cols: int, fmt: int, xq, xd, xs, T: int, i
                                            _ptr(margin), _ptr(logits), _ptr(workspace), ws_bytes, _stream(stream)),
            "strata_head_argmax_margin")
     return ids, margin
+
+
+def gemm_q4(W, rows: int, cols: int, xq, xd, y=None, stream=None):
+    """y fp32 [n_tok][rows] = the block-quantized product of n_tok activation rows with a Q4 matrix."""
+    n_tok = xq.shape[0]
+    if y is None:
+        y = torch.empty((n_tok, rows), dtype=torch.float32, device=xq.device)
+    _check(lib().strata_gemm_q4(_ptr(W), rows, cols, _ptr(xq), _ptr(xd), n_tok, _ptr(y), _stream(stream)),
+           "strata_gemm_q4")
+    return y
 
 
 def block_dots(W, rows: int, cols: int, fmt: int, xq, xs, T: int, isum=None, stream=None):

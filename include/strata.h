@@ -202,6 +202,23 @@ int strata_head_argmax_noalloc(const void* W, int64_t vocab, int64_t cols, int f
                                int32_t* ids, float* logits, cudaStream_t stream);
 
 /*
+ * strata_gemm_q4 — dense prompt-chunk GEMM: n_tok quantized activation rows against one Q4 matrix on
+ * the tensor cores (tcgen05, fp16 operands holding the exact codes, one TMEM accumulator per quant
+ * block). The prompt path of the Strata pull request "sm_80 (GA100) tuning" multiplies whole prompt
+ * chunks with the dense quantized weights (it dequantizes them every chunk); here the integer
+ * block dots stay exact and the block arithmetic is the GEMV's:
+ *     y[n][r] = sum_b (d_w[r][b] * xd[n][b]) * isum[n][r][b]        (fp32, block order)
+ *   W : Q4 [rows][cols] (planar layout above).  xq int8 [n_tok][cols], xd fp32 [n_tok][cols/32]: from
+ *   strata_quantize_act (the block sums are not needed).  y : fp32 [n_tok][rows], fully written.
+ *   rows % 128 == 0, cols % 64 == 0, rows and cols <= 65536, 1 <= n_tok <= 2^24. W, xq, y 16-byte
+ *   aligned, xd 4-byte aligned. Outputs are within the fp32 bound of the exact values; the summation
+ *   order differs from strata_mmvq_multi's, so the two agree within the bound, not bit for bit.
+ *   Errors: NULL, SHAPE, ALIGN, CUDA; a timed-out wait sets bit 0 of the device error word.
+ */
+int strata_gemm_q4(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                   int64_t n_tok, float* y, cudaStream_t stream);
+
+/*
  * strata_moe_grouped — prompt-chunk MoE experts: per (token, slot) pair p = tok*k + slot routed to
  * expert e = ids[p]:
  *     g = W_gate[e] . xq(tok), u = W_up[e] . xq(tok)         (block arithmetic above, fp32)

@@ -109,3 +109,18 @@ def test_moe_debug_views(L):
     vals = list(out)
     assert vals == sorted(vals) and all(v % 256 == 0 for v in vals)
     assert vals[6] == L.strata_moe_grouped_workspace(128, 3256, 8, 2048, 768)
+
+
+def test_gemm_rejects(L):
+    ok = [A16, 256, 512, A16, A16, 300, A16, None]
+    assert L.strata_gemm_q4(*ok[:0], None, 256, 512, A16, A16, 300, A16, None) == -1
+    a = list(ok); a[1] = 200
+    assert L.strata_gemm_q4(*a) == -2                 # rows % 128
+    a = list(ok); a[2] = 96
+    assert L.strata_gemm_q4(*a) == -2                 # cols % 64
+    a = list(ok); a[5] = 0
+    assert L.strata_gemm_q4(*a) == -2                 # no rows of activations
+    a = list(ok); a[3] = A16 + 8
+    assert L.strata_gemm_q4(*a) == -7                 # xq alignment
+    a = list(ok); a[6] = A16 + 4
+    assert L.strata_gemm_q4(*a) == -7                 # y alignment
