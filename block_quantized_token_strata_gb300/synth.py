@@ -9,6 +9,8 @@ Distributions (the workload recipe):
   * weight block scales d = fp16(|N(0,1)| * 0.01), rounded to nearest-even by numpy;
   * Q4 codes q ~ U{0..15} (two independent codes per byte, i.e. a uniform byte);
   * Q8 codes q ~ U{-127..127};
+  * Q6 (256-weight super-blocks): codes q ~ U{0..63}, sub-block scales ~ U{-127..127} (int8, one
+    per 16 weights), super-block scale d = fp16(|N(0,1)| * 0.001);
   * activations x ~ N(0,1) fp32, optionally with a Bernoulli(0.01) mask of elements scaled x20;
   * MoE routing: k distinct experts per token drawn without replacement from a Zipf(1.1)
     law over expert ranks, p_e proportional to (e+1)^-1.1, draw order = slot order.
@@ -20,8 +22,9 @@ import hashlib
 import numpy as np
 
 QK = 32
-Q4, Q8 = 0, 1
-_QBYTES = {Q4: 16, Q8: 32}
+QKS = 256  # Q6 super-block
+Q4, Q8, Q6 = 0, 1, 2
+_QBYTES = {Q4: 16, Q8: 32, Q6: 24}
 
 
 def _rng(*key) -> np.random.Generator:
@@ -37,7 +40,8 @@ def _rng(*key) -> np.random.Generator:
 
 def weight_nbytes(rows: int, cols: int, fmt: int) -> int:
     nb = rows * (cols // QK)
-    return nb * (_QBYTES[fmt] + 2)
+    extra = rows * (cols // QKS) * 2 if fmt == Q6 else 0   # Q6: one fp16 d per super-block
+    return nb * (_QBYTES[fmt] + 2) + extra
 
 
 class Weights:
@@ -70,11 +74,33 @@ class Weights:
         return out.reshape(r1 - r0, self.cols)
 
 
+def make_q6_buffer(q: np.ndarray, sub: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Lay out Q6 codes q uint8 [rows][cols] (0..63), sub-block scales int8 [rows][cols/16] and
+    super-block scales fp16 [rows][cols/256] in the planar Q6 format of include/strata.h."""
+    rows, cols = q.shape
+    nb = cols // QK
+    qb = q.reshape(rows, nb, 32).astype(np.uint8)
+    low = (qb & 15)
+    high = (qb >> 4) & 3
+    code = np.empty((rows, nb, 24), np.uint8)
+    code[:, :, :16] = low[:, :, :16] | (low[:, :, 16:] << 4)
+    code[:, :, 16:] = high[:, :, 0:8] | (high[:, :, 8:16] << 2) | (high[:, :, 16:24] << 4) | (high[:, :, 24:32] << 6)
+    return np.concatenate([code.reshape(-1), np.asarray(sub, np.int8).reshape(-1).view(np.uint8),
+                           np.asarray(d, np.float16).reshape(-1).view(np.uint8)])
+
+
 def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
-    """A seeded [rows][cols] matrix in Q4 or Q8 (planar layout, see include/strata.h)."""
+    """A seeded [rows][cols] matrix in Q4, Q8 or Q6 (planar layout, see include/strata.h)."""
     if cols % QK or rows <= 0:
         raise ValueError("cols must be a multiple of 32 and rows positive")
     rng = _rng("weights", rows, cols, fmt, *key)
+    if fmt == Q6:
+        if cols % QKS:
+            raise ValueError("Q6 needs cols % 256 == 0")
+        q = rng.integers(0, 64, size=(rows, cols), dtype=np.uint8)
+        sub = rng.integers(-127, 128, size=(rows, cols // 16), dtype=np.int8)
+        d = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
+        return Weights(rows, cols, fmt, make_q6_buffer(q, sub, d))
     nb = rows * (cols // QK)
     d = (np.abs(rng.standard_normal(nb)) * 0.01).astype(np.float16)
     if fmt == Q4:

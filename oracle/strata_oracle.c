@@ -17,7 +17,9 @@
  *     lowest id.
  * Readings where the pages are silent (block formats, the quantizer, the MoE hidden activation):
  *   Q4 block = fp16 d + 32 unsigned 4-bit codes, w = d*(q-8); Q8 block = fp16 d + 32 int8 codes,
- *   w = d*q; activations: per 32 values amax, d = amax/127 (fp32), q = roundf(x/d) via x*(1/d),
+ *   w = d*q; Q6 (the pages' 6-bit super-block type, 210 bytes per 256 weights): per 256 weights an
+ *   fp16 d, per 16 weights an int8 sub-scale s, 6-bit codes q, w = d*s*(q-32), with exact integer
+ *   dots per 16 weights (one term per sub-scale); activations: per 32 values amax, d = amax/127 (fp32), q = roundf(x/d) via x*(1/d),
  *   s = sum q; MoE hidden h = silu(g)*u with silu(g) = g/(1+exp(-g)), re-quantized the same way.
  *
  * Arithmetic: integer dots in int64 (exact); block terms d_w * d_x * isum and all sums in fp64, in
@@ -34,6 +36,7 @@
 
 #define OR_Q4 0
 #define OR_Q8 1
+#define OR_Q6 2
 
 /* ---- IEEE 754 binary16 -> double, from the format's definition ---------------------------- */
 double or_half_to_double(uint16_t h)
@@ -53,13 +56,25 @@ double or_half_to_double(uint16_t h)
 }
 
 /* ---- the planar weight layout ---------------------------------------------------------------- */
-static int64_t qbytes(int fmt) { return fmt == OR_Q4 ? 16 : 32; }
+static int64_t qbytes(int fmt) { return fmt == OR_Q4 ? 16 : (fmt == OR_Q8 ? 32 : 24); }
 
+/* Q4/Q8: the fp16 scale of block (r, b). Q6: the fp16 d of the super-block holding block b, which
+ * sits after the code plane (24 bytes a block) and the sub-scale plane (2 int8 a block). */
 static double block_scale(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t r, int64_t b)
 {
-    const uint8_t* p = W + rows * nb * qbytes(fmt) + 2 * (r * nb + b);
+    const uint8_t* p;
+    if (fmt == OR_Q6)
+        p = W + rows * nb * 26 + 2 * (r * (nb / 8) + b / 8);
+    else
+        p = W + rows * nb * qbytes(fmt) + 2 * (r * nb + b);
     uint16_t bits = (uint16_t)(p[0] | (p[1] << 8));
     return or_half_to_double(bits);
+}
+
+/* Q6: the int8 sub-scale of half h (elements 16h..16h+15) of block (r, b) */
+static int q6_subscale(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, int64_t b, int h)
+{
+    return (int)(int8_t)W[rows * nb * 24 + 2 * (r * nb + b) + h];
 }
 
 /* weight code of element j (0..31) of block (r, b), already offset: Q4 q-8, Q8 q */
@@ -70,6 +85,15 @@ static int weight_code(const uint8_t* W, int64_t nb, int fmt, int64_t r, int64_t
         int byte = blk[j & 15];
         int q = (j < 16) ? (byte & 0x0F) : (byte >> 4);
         return q - 8;
+    }
+    if (fmt == OR_Q6) {
+        /* bytes 0..15: low 4 bits of element j (low nibble) and of element j+16 (high nibble);
+         * bytes 16..23: byte 16+i holds the high 2 bits of elements i, i+8, i+16, i+24 (bits 0-1, 2-3,
+         * 4-5, 6-7); the code q = low | high << 4 in 0..63 stands for q - 32 */
+        int byte = blk[j & 15];
+        int low = (j < 16) ? (byte & 0x0F) : (byte >> 4);
+        int high = (blk[16 + (j & 7)] >> (2 * (j >> 3))) & 3;
+        return (low | (high << 4)) - 32;
     }
     return (int)(int8_t)blk[j];
 }
@@ -102,12 +126,22 @@ void or_quantize_act(const float* x, int64_t n, int64_t cols, int8_t* q, float* 
 }
 
 /* ---- exact integer block dot ------------------------------------------------------------------ */
-static int64_t block_isum(const uint8_t* W, int64_t nb, int fmt, int64_t r, int64_t b, const int8_t* xq_blk)
+static int64_t half_isum(const uint8_t* W, int64_t nb, int fmt, int64_t r, int64_t b, const int8_t* xq_blk, int h)
 {
     int64_t acc = 0;
-    for (int j = 0; j < 32; ++j)
+    for (int j = 16 * h; j < 16 * h + 16; ++j)
         acc += (int64_t)weight_code(W, nb, fmt, r, b, j) * (int64_t)xq_blk[j];
     return acc;
+}
+
+/* the block's exact integer dot; Q6: sub-scale-weighted, s0 * (first 16) + s1 * (last 16) */
+static int64_t block_isum(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t r, int64_t b,
+                          const int8_t* xq_blk)
+{
+    if (fmt == OR_Q6)
+        return q6_subscale(W, rows, nb, r, b, 0) * half_isum(W, nb, fmt, r, b, xq_blk, 0) +
+               q6_subscale(W, rows, nb, r, b, 1) * half_isum(W, nb, fmt, r, b, xq_blk, 1);
+    return half_isum(W, nb, fmt, r, b, xq_blk, 0) + half_isum(W, nb, fmt, r, b, xq_blk, 1);
 }
 
 /* isum[t][r][b] for every token, row and block (int64) */
@@ -119,7 +153,7 @@ void or_block_dots(const uint8_t* W, int64_t rows, int64_t cols, int fmt, const 
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t t = 0; t < T; ++t)
             for (int64_t b = 0; b < nb; ++b)
-                isum[(t * rows + r) * nb + b] = block_isum(W, nb, fmt, r, b, xq + t * cols + 32 * b);
+                isum[(t * rows + r) * nb + b] = block_isum(W, rows, nb, fmt, r, b, xq + t * cols + 32 * b);
 }
 
 /* one output: y = sum_b d_w * d_x * isum in fp64, block order; A = sum_b |term| */
@@ -128,7 +162,17 @@ static void row_dot(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t
 {
     double acc = 0.0, aabs = 0.0;
     for (int64_t b = 0; b < nb; ++b) {
-        int64_t isum = block_isum(W, nb, fmt, r, b, xq_row + 32 * b);
+        if (fmt == OR_Q6) {  /* one term per 16 weights: d * s_h * d_x * isum_h */
+            for (int h = 0; h < 2; ++h) {
+                int64_t isum = half_isum(W, nb, fmt, r, b, xq_row + 32 * b, h);
+                double term = block_scale(W, rows, nb, fmt, r, b) * (double)q6_subscale(W, rows, nb, r, b, h) *
+                              (double)xd_row[b] * (double)isum;
+                acc += term;
+                aabs += fabs(term);
+            }
+            continue;
+        }
+        int64_t isum = block_isum(W, rows, nb, fmt, r, b, xq_row + 32 * b);
         double term = block_scale(W, rows, nb, fmt, r, b) * (double)xd_row[b] * (double)isum;
         acc += term;
         aabs += fabs(term);

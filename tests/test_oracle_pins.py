@@ -296,3 +296,67 @@ def test_margin_matches_two_shard_merge(orc):
         a1, a2, b1, b2 = A[0], A[1], B[0], B[1]
         second = max(a2, b1) if a1 >= b1 else max(b2, a1)
         assert oracle.margin(row)[0] == max(a1, b1) - second
+
+
+# ---- Q6 (6-bit codes, int8 sub-scale per 16 weights, fp16 d per 256 weights) --------------------------
+def pack_q6(q: np.ndarray, sub: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """This test's own packer of the documented Q6 planar layout (code plane 24 B a block: bytes 0..15
+    the low 4 bits of elements j and j+16, bytes 16..23 the high 2 bits of elements i, i+8, i+16,
+    i+24; then int8 sub-scales, 2 a block; then fp16 d, one per 256 weights)."""
+    rows, cols = q.shape
+    nb = cols // 32
+    out = bytearray()
+    for r in range(rows):
+        for b in range(nb):
+            blk = [int(v) for v in q[r, 32 * b:32 * b + 32]]
+            low = [blk[j] & 15 for j in range(32)]
+            high = [blk[j] >> 4 for j in range(32)]
+            out += bytes(low[j] | (low[j + 16] << 4) for j in range(16))
+            out += bytes(high[i] | (high[i + 8] << 2) | (high[i + 16] << 4) | (high[i + 24] << 6) for i in range(8))
+    out += np.asarray(sub, np.int8).tobytes()
+    out += np.asarray(d, np.float16).tobytes()
+    return np.frombuffer(bytes(out), np.uint8).copy()
+
+
+def test_q6_one_superblock_by_hand(orc):
+    """cols = 256 (one super-block, 8 blocks, 16 sub-scales); d = 1, x codes all 1 with d_x = 1:
+    codes all 32 give 0; codes all 63 with sub-scales 1 give 16 halves x 16 x 31 = 7936; sub-scales
+    alternating +1/-1 cancel to 0; sub-scale 3 on the first half only gives 3 x 16 x 31 = 1488."""
+    xq = np.ones((1, 256), np.int8)
+    xd = np.ones((1, 8), np.float32)
+    d = np.ones((1, 1), np.float16)
+    cases = [(32, np.ones(16), 0.0), (63, np.ones(16), 7936.0),
+             (63, np.array([1, -1] * 8), 0.0), (63, np.array([3] + [0] * 15), 1488.0)]
+    for code, sub, want in cases:
+        W = pack_q6(np.full((1, 256), code, np.uint8), sub.reshape(1, 16).astype(np.int8), d)
+        y, A = orc.mmvq(W, 1, 256, 2, xq, xd)
+        assert y[0, 0] == want, (code, sub, y)
+
+
+def test_q6_brute_force_dense(orc):
+    """Dense fp64 dequantization w = d * s * (q - 32) against the oracle's block form."""
+    rng = np.random.default_rng(17)
+    rows, cols, T = 9, 768, 3
+    q = rng.integers(0, 64, size=(rows, cols)).astype(np.uint8)
+    sub = rng.integers(-127, 128, size=(rows, cols // 16)).astype(np.int8)
+    d = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+    W = pack_q6(q, sub, d)
+    assert W.size == rows * (cols // 256) * 210
+    x = rng.standard_normal((T, cols)).astype(np.float32)
+    xq, xd, _ = orc.quantize_act(x)
+    w = (d.astype(np.float64).repeat(256, axis=1) * sub.astype(np.float64).repeat(16, axis=1)
+         * (q.astype(np.float64) - 32))
+    xdq = xq.astype(np.float64) * xd.astype(np.float64).repeat(32, axis=1)
+    ref = xdq @ w.T
+    y, A = orc.mmvq(W, rows, cols, 2, xq, xd)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # the block dots: s0 * (first 16) + s1 * (last 16), brute force in int64
+    isum = orc.block_dots(W, rows, cols, 2, xq)
+    qq = q.astype(np.int64).reshape(rows, cols // 32, 2, 16) - 32
+    ss = sub.astype(np.int64).reshape(rows, cols // 32, 2)
+    xx = xq.astype(np.int64).reshape(T, cols // 32, 2, 16)
+    want = np.einsum("rbhj,tbhj,rbh->trb", qq, xx, ss)
+    assert np.array_equal(isum.reshape(T, rows, cols // 32), want)
+    # the generator's buffer decodes the same way
+    from block_quantized_token_strata_gb300 import synth
+    assert np.array_equal(synth.make_q6_buffer(q, sub, d), W)
