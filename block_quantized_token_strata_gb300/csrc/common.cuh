@@ -147,6 +147,29 @@ __device__ __forceinline__ int dot_q8(const uint4 w0, const uint4 w1, const uint
     c = __dp4a(int(w1.w), int(xhi.w), c);
     return c;
 }
+// Q6 block codes as dp4a operands: words 0..3 hold elements 0..15, words 4..7 elements 16..31, one
+// 6-bit code q (0..63) per byte. Layout: lo0/lo1 = code bytes 0..15 (byte j: low 4 bits of element j
+// in bits 0-3, of element j+16 in bits 4-7), hi = bytes 16..23 (byte 16+i: the high 2 bits of
+// elements i, i+8, i+16, i+24 in bits 0-1, 2-3, 4-5, 6-7).
+__device__ __forceinline__ void unpack_q6(const uint2 lo0, const uint2 lo1, const uint2 hi, uint32_t (&q)[8]) {
+    const uint32_t L[4] = {lo0.x, lo0.y, lo1.x, lo1.y};
+    q[0] = (L[0] & 0x0F0F0F0Fu) | ((hi.x & 0x03030303u) << 4);
+    q[1] = (L[1] & 0x0F0F0F0Fu) | ((hi.y & 0x03030303u) << 4);
+    q[2] = (L[2] & 0x0F0F0F0Fu) | ((hi.x & 0x0C0C0C0Cu) << 2);
+    q[3] = (L[3] & 0x0F0F0F0Fu) | ((hi.y & 0x0C0C0C0Cu) << 2);
+    q[4] = ((L[0] >> 4) & 0x0F0F0F0Fu) | (hi.x & 0x30303030u);
+    q[5] = ((L[1] >> 4) & 0x0F0F0F0Fu) | (hi.y & 0x30303030u);
+    q[6] = ((L[2] >> 4) & 0x0F0F0F0Fu) | ((hi.x & 0xC0C0C0C0u) >> 2);
+    q[7] = ((L[3] >> 4) & 0x0F0F0F0Fu) | ((hi.y & 0xC0C0C0C0u) >> 2);
+}
+// 16 codes (4 words) against 16 activation codes, onto c
+__device__ __forceinline__ int dot16(const uint32_t* q, const uint4 x, int c) {
+    c = __dp4a(int(q[0]), int(x.x), c);
+    c = __dp4a(int(q[1]), int(x.y), c);
+    c = __dp4a(int(q[2]), int(x.z), c);
+    c = __dp4a(int(q[3]), int(x.w), c);
+    return c;
+}
 // ---- packed fp32 pairs (sm_100+): each half is one IEEE fp32 operation, rounded to nearest --------
 typedef unsigned long long f32x2;
 __device__ __forceinline__ f32x2 pack_f2(float lo, float hi) {

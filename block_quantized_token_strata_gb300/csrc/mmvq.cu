@@ -80,6 +80,9 @@ __device__ int g_strata_device_error = 0;
 template <int FMT> struct FmtInfo;
 template <> struct FmtInfo<0> { static constexpr int kQB = 16; };  // Q4: 16 code bytes per block
 template <> struct FmtInfo<1> { static constexpr int kQB = 32; };  // Q8: 32 code bytes per block
+// Q6: 24 code bytes per block (16 of low 4-bit parts, 8 of high 2-bit parts); its "scale plane" holds
+// the two int8 sub-scales of each block, and a third plane one fp16 d per 8 blocks (256 weights)
+template <> struct FmtInfo<2> { static constexpr int kQB = 24; };
 
 struct GemvMat {
     const uint8_t* W;
@@ -98,6 +101,7 @@ struct GemvParams {
     int n_chunk;     // row groups over all matrices
     int cstage;      // bytes per stage in the code ring (multiple of 128)
     int sstage;      // bytes per stage in the scale ring (multiple of 128, 32 bytes of slack)
+    int dstage;      // Q6: bytes per stage in the super-block scale ring (multiple of 128, 32 of slack)
     int nst;         // stages in the ring (1..32)
     int nb_max;      // widest matrix, for the activation copy
     int pf;          // stages the producer prefetches into L2 ahead of its bulk copies
@@ -156,16 +160,19 @@ template <int N> struct Pow2Ceil { static constexpr int v = N <= 1 ? 1 : 2 * Pow
 // then high half, token after token), then T scales and T dp4a seeds (each padded to TPP). The
 // record size is 16 mod 32 bytes, so lanes reading consecutive blocks hit distinct bank groups, and
 // every token's operand sits at an immediate offset from one per-block address.
-template <int T>
+// Q6 records hold two seeds a token (one per 16-code half) after the scales. The size is a multiple
+// of 16 (every record starts on a 16-byte boundary for the 16-byte code loads and stores).
+template <int T, int FMT>
 struct XRec {
     static constexpr int tpp = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
-    static constexpr int raw = T * 32 + tpp * 8;
+    static constexpr int raw = (T * 32 + tpp * (FMT == 2 ? 12 : 8) + 15) / 16 * 16;
     static constexpr int bytes = (raw % 32 == 0) ? raw + 16 : raw;
+    static_assert(bytes % 16 == 0 && bytes % 32 == 16, "activation records: 16 mod 32 bytes");
 };
-static int xrec_bytes(int T)
+static int xrec_bytes(int T, int fmt)
 {
     const int tpp = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
-    const int raw = T * 32 + tpp * 8;
+    const int raw = (T * 32 + tpp * (fmt == 2 ? 12 : 8) + 15) / 16 * 16;
     return (raw % 32 == 0) ? raw + 16 : raw;
 }
 template <> struct Pow2Ceil<1> { static constexpr int v = 1; };
@@ -224,7 +231,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     constexpr int V = Pow2Ceil<kR * T>::v;
     constexpr int TPP = T <= 2 ? 2 : (T <= 4 ? 4 : 8);  // tokens padded for the scale vectors
     constexpr int NP = (T + 1) / 2;                      // token pairs
-    constexpr int RX = XRec<T>::bytes;                   // activation record per block
+    constexpr int RX = XRec<T, FMT>::bytes;              // activation record per block
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int s_abort;
 
@@ -238,6 +245,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     uint8_t* cring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(hs + kCW * 32) + 127) & ~uintptr_t(127));   // codes [NST][cstage]
     uint8_t* sring = cring + NST * p.cstage;                                      // scales [NST][sstage]
+    uint8_t* dring = sring + NST * p.sstage;                                      // Q6 d [NST][dstage]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int g0, g1;  // this CTA's chunks
@@ -277,6 +285,12 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 const uintptr_t sa = reinterpret_cast<uintptr_t>(m.W + size_t(m.rows) * m.nb * QB + size_t(r0) * m.nb * 2);
                 const uintptr_t lo = (sa + 15) & ~uintptr_t(15), hi2 = (sa + uint32_t(nr) * m.nb * 2) & ~uintptr_t(15);
                 if (hi2 > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), uint32_t(hi2 - lo));
+                if constexpr (FMT == 2) {
+                    const uintptr_t da = reinterpret_cast<uintptr_t>(m.W + size_t(m.rows) * m.nb * (QB + 2) +
+                                                                     size_t(r0) * (m.nb / 8) * 2);
+                    const uintptr_t dlo = (da + 15) & ~uintptr_t(15), dhi = (da + uint32_t(nr) * (m.nb / 8) * 2) & ~uintptr_t(15);
+                    if (dhi > dlo) bulk_prefetch_l2(reinterpret_cast<const void*>(dlo), uint32_t(dhi - dlo));
+                }
                 pf.next();
             };
             for (int q = 0; q < p.pf; ++q) prefetch_next();
@@ -310,11 +324,30 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 const uint32_t tail = sbytes - head - mid;
                 for (uint32_t b = 0; b < head; ++b) sdst[b] = __ldg(ssrc + b);
                 for (uint32_t b = sbytes - tail; b < sbytes; ++b) sdst[b] = __ldg(ssrc + b);
+                // Q6: the super-block scales of the same rows, placed like the scales (same alignment
+                // mod 16 as the source; the unaligned ends by plain loads)
+                const uint8_t* dsrc = nullptr;
+                uint8_t* ddst = nullptr;
+                uint32_t dhead = 0, dmid = 0;
+                if constexpr (FMT == 2) {
+                    const int ns = m.nb / 8;
+                    dsrc = m.W + size_t(m.rows) * m.nb * (QB + 2) + size_t(r0) * ns * 2;
+                    const uint32_t dbytes = uint32_t(nr) * ns * 2;
+                    const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dsrc) & 15);
+                    ddst = dring + s * p.dstage + dmis;
+                    dhead = min(dbytes, (16u - dmis) & 15u);
+                    dmid = (dbytes - dhead) & ~15u;
+                    const uint32_t dtail = dbytes - dhead - dmid;
+                    for (uint32_t b = 0; b < dhead; ++b) ddst[b] = __ldg(dsrc + b);
+                    for (uint32_t b = dbytes - dtail; b < dbytes; ++b) ddst[b] = __ldg(dsrc + b);
+                    if (dhead | dtail) fence_proxy_async_smem();
+                }
                 if (head | tail) fence_proxy_async_smem();
                 const uint32_t fb = smem_u32(&bars[s]);
-                mbar_arrive_expect_tx(fb, qbytes + mid);
+                mbar_arrive_expect_tx(fb, qbytes + mid + dmid);
                 bulk_g2s(smem_u32(cring + s * p.cstage), qsrc, qbytes, fb, pol);
                 if (mid) bulk_g2s(smem_u32(sdst + head), ssrc + head, mid, fb, pol);
+                if (dmid) bulk_g2s(smem_u32(ddst + dhead), dsrc + dhead, dmid, fb, pol);
             }
             if (!waited) {
                 pdl_wait();
@@ -363,13 +396,27 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
             for (int i = threadIdx.x; i < nb * TPP; i += kCW * 32) {
                 const int b = i / TPP, t = i - (i / TPP) * TPP;
                 float d = 0.0f;
-                int c0 = kMagicBits;
+                int c0 = kMagicBits, c1 = kMagicBits;
                 if (t < T) {
                     d = __ldg(m.xd + t * nb + b);
                     if (FMT == 0) c0 = kMagicBits - 8 * __ldg(m.xs + t * nb + b);
+                    if (FMT == 2) {
+                        // Q6 codes stand for q - 32 and carry one sub-scale per 16: seed each half's chain
+                        // with -32 times that half's activation sum
+                        const uint4* xb = src + size_t(t) * nb * 2 + size_t(b) * 2;
+                        const uint4 lo = __ldg(xb), hi = __ldg(xb + 1);
+                        int sl = 0, sh = 0;
+                        sl = __dp4a(int(lo.x), 0x01010101, sl); sl = __dp4a(int(lo.y), 0x01010101, sl);
+                        sl = __dp4a(int(lo.z), 0x01010101, sl); sl = __dp4a(int(lo.w), 0x01010101, sl);
+                        sh = __dp4a(int(hi.x), 0x01010101, sh); sh = __dp4a(int(hi.y), 0x01010101, sh);
+                        sh = __dp4a(int(hi.z), 0x01010101, sh); sh = __dp4a(int(hi.w), 0x01010101, sh);
+                        c0 = kMagicBits - 32 * sl;
+                        c1 = kMagicBits - 32 * sh;
+                    }
                 }
                 *reinterpret_cast<float*>(xsm + b * RX + T * 32 + t * 4) = d;
                 *reinterpret_cast<int*>(xsm + b * RX + T * 32 + TPP * 4 + t * 4) = c0;
+                if (FMT == 2) *reinterpret_cast<int*>(xsm + b * RX + T * 32 + TPP * 8 + t * 4) = c1;
             }
         }
         named_bar_sync(1, kCW * 32);
@@ -416,6 +463,70 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                     for (int r = 0; r < kR; ++r)
 #pragma unroll
                         for (int q = 0; q < NP; ++q) acc[r][q] = 0ull;
+                    if constexpr (FMT == 2) {
+                        // Q6: per block 24 code bytes, two int8 sub-scales, the super-block's fp16 d
+                        const uintptr_t dsrc = reinterpret_cast<uintptr_t>(m.W + size_t(rows) * nb * (QB + 2) +
+                                                                           size_t(r0s) * (nb / 8) * 2);
+                        const unsigned short* dpl = reinterpret_cast<const unsigned short*>(
+                            dring + s * p.dstage + int(dsrc & 15) + pos * (kR * 2) * (nb / 8));
+                        const int ns = nb / 8;
+                        for (int kb = gl; kb < nb; kb += G) {
+                            const uint8_t* wp = cb + kb * QB;
+                            const unsigned short* sp = sc + kb;
+                            const uint8_t* xr = xsm + kb * RX;
+                            uint2 wl0[kR], wl1[kR], wh[kR];
+                            f32x2 sdl2[kR], sdh2[kR];
+#pragma unroll
+                            for (int r = 0; r < kR; ++r) {
+                                wl0[r] = *reinterpret_cast<const uint2*>(wp + r * rsw);
+                                wl1[r] = *reinterpret_cast<const uint2*>(wp + r * rsw + 8);
+                                wh[r] = *reinterpret_cast<const uint2*>(wp + r * rsw + 16);
+                                const unsigned short su = sp[r * nb];
+                                const float dd = __half2float(__ushort_as_half(dpl[r * ns + (kb >> 3)]));
+                                // d * s is exact in fp32 (11 + 7 significant bits)
+                                const float s0 = __fmul_rn(dd, float(int(int8_t(su & 0xFF))));
+                                const float s1 = __fmul_rn(dd, float(int(int8_t(su >> 8))));
+                                sdl2[r] = pack_f2(s0, s0);
+                                sdh2[r] = pack_f2(s1, s1);
+                            }
+                            float dxv[TPP];
+                            int c0v[TPP], c1v[TPP];
+#pragma unroll
+                            for (int q = 0; q < TPP; q += 2) {
+                                const float2 dd = *reinterpret_cast<const float2*>(xr + T * 32 + q * 4);
+                                const int2 cc = *reinterpret_cast<const int2*>(xr + T * 32 + TPP * 4 + q * 4);
+                                const int2 ch = *reinterpret_cast<const int2*>(xr + T * 32 + TPP * 8 + q * 4);
+                                dxv[q] = dd.x; dxv[q + 1] = dd.y;
+                                c0v[q] = cc.x; c0v[q + 1] = cc.y;
+                                c1v[q] = ch.x; c1v[q + 1] = ch.y;
+                            }
+#pragma unroll
+                            for (int q = 0; q < NP; ++q) {
+                                const int ta = 2 * q, tb = 2 * q + 1;
+                                const uint4 xla = *reinterpret_cast<const uint4*>(xr + ta * 32);
+                                const uint4 xha = *reinterpret_cast<const uint4*>(xr + ta * 32 + 16);
+                                uint4 xlb = xla, xhb = xha;
+                                if (tb < T) {
+                                    xlb = *reinterpret_cast<const uint4*>(xr + tb * 32);
+                                    xhb = *reinterpret_cast<const uint4*>(xr + tb * 32 + 16);
+                                }
+                                const f32x2 dx2 = pack_f2(dxv[ta], dxv[tb]);
+#pragma unroll
+                                for (int r = 0; r < kR; ++r) {
+                                    uint32_t qw[8];
+                                    unpack_q6(wl0[r], wl1[r], wh[r], qw);
+                                    const int la = dot16(qw, xla, c0v[ta]), ha = dot16(qw + 4, xha, c1v[ta]);
+                                    const int lb = (tb < T) ? dot16(qw, xlb, c0v[tb]) : kMagicBits;
+                                    const int hb = (tb < T) ? dot16(qw + 4, xhb, c1v[tb]) : kMagicBits;
+                                    // one term per sub-scale, the low half first: acc += (d*s*d_x) * isum_half
+                                    const f32x2 fl = add_f2(pack_f2(__int_as_float(la), __int_as_float(lb)), negm);
+                                    const f32x2 fh = add_f2(pack_f2(__int_as_float(ha), __int_as_float(hb)), negm);
+                                    acc[r][q] = fma_f2(mul_f2(sdl2[r], dx2), fl, acc[r][q]);
+                                    acc[r][q] = fma_f2(mul_f2(sdh2[r], dx2), fh, acc[r][q]);
+                                }
+                            }
+                        }
+                    } else {
                     for (int kb = gl; kb < nb; kb += G) {
                         const uint8_t* wp = cb + kb * QB;
                         const unsigned short* sp = sc + kb;
@@ -466,6 +577,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                             }
                         }
                     }
+                    }  // Q4 / Q8
 #pragma unroll
                     for (int r = 0; r < kR; ++r)
 #pragma unroll
@@ -592,6 +704,27 @@ __global__ void __launch_bounds__(256) block_dots_kernel(const uint8_t* __restri
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= int64_t(rows) * nb) return;
     const int r = int(i / nb), b = int(i % nb);
+    if constexpr (FMT == 2) {
+        // Q6: s0 * sum over the first 16 of (q-32)*x + s1 * the same over the last 16 (exact int)
+        const uint8_t* blk = W + size_t(i) * 24;
+        const uint2 lo0 = *reinterpret_cast<const uint2*>(blk), lo1 = *reinterpret_cast<const uint2*>(blk + 8);
+        const uint2 hi = *reinterpret_cast<const uint2*>(blk + 16);
+        const unsigned short su = *reinterpret_cast<const unsigned short*>(W + size_t(rows) * nb * 24 + size_t(i) * 2);
+        uint32_t qw[8];
+        unpack_q6(lo0, lo1, hi, qw);
+        for (int t = 0; t < T; ++t) {
+            const uint4* xp = reinterpret_cast<const uint4*>(xq + size_t(t) * nb * 32 + size_t(b) * 32);
+            const uint4 xl = xp[0], xh = xp[1];
+            int sl = 0, sh = 0;
+            sl = __dp4a(int(xl.x), 0x01010101, sl); sl = __dp4a(int(xl.y), 0x01010101, sl);
+            sl = __dp4a(int(xl.z), 0x01010101, sl); sl = __dp4a(int(xl.w), 0x01010101, sl);
+            sh = __dp4a(int(xh.x), 0x01010101, sh); sh = __dp4a(int(xh.y), 0x01010101, sh);
+            sh = __dp4a(int(xh.z), 0x01010101, sh); sh = __dp4a(int(xh.w), 0x01010101, sh);
+            const int l = dot16(qw, xl, -32 * sl), h = dot16(qw + 4, xh, -32 * sh);
+            isum[(size_t(t) * rows + r) * nb + b] = int(int8_t(su & 0xFF)) * l + int(int8_t(su >> 8)) * h;
+        }
+        return;
+    }
     const uint4 w0 = ld_stream_v4(W + size_t(i) * QB);
     const uint4 w1 = (QB == 32) ? ld_stream_v4(W + size_t(i) * QB + 16) : w0;
     for (int t = 0; t < T; ++t) {
@@ -618,7 +751,9 @@ int device_sm_count()
     return cache[dev];
 }
 
-static int qbytes_of(int fmt) { return fmt == 0 ? 16 : 32; }
+static int qbytes_of(int fmt) { return fmt == 0 ? 16 : (fmt == 1 ? 32 : 24); }
+// weight bytes per row group beyond the codes and the per-block 2-byte plane: Q6's super-block d
+static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : 0; }
 
 // Warps per row: a function of (cols, fmt) only, so every launch of a shape (any T, single or
 // grouped) sums each row in the same order. As few warps as keep at least two blocks per lane
@@ -636,7 +771,7 @@ int gemv_warps_per_row(int64_t cols, int fmt)
 // stage), about STRATA_STAGE_KB of codes and scales; a power of two when STRATA_SG_POW2 is set.
 static int stage_chunks(int64_t cols, int fmt, int ks)
 {
-    const int64_t chunk = int64_t(kR) * (cols / kQK) * (qbytes_of(fmt) + 2);
+    const int64_t chunk = int64_t(kR) * ((cols / kQK) * (qbytes_of(fmt) + 2) + dbytes_per_row(cols, fmt));
     const int ng = kCW / ks;
     if (STRATA_SG_POW2) {
         int l = 0;
@@ -648,7 +783,7 @@ static int stage_chunks(int64_t cols, int fmt, int ks)
 }
 
 struct Plan {
-    int cstage, sstage, ns, nb_max;
+    int cstage, sstage, dstage, ns, nb_max;
     size_t smem;
 };
 
@@ -661,21 +796,23 @@ constexpr int kPrefetchStages = STRATA_PF_STAGES;
 static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
 {
     Plan pl;
-    size_t cmax = 0, smax = 0;
+    size_t cmax = 0, smax = 0, dmax = 0;
     int nb_max = 0;
     for (int i = 0; i < n; ++i) {
         const size_t rows = size_t(ms[i].sg) * kR;
         cmax = std::max(cmax, rows * ms[i].nb * qbytes_of(fmt));
         smax = std::max(smax, rows * ms[i].nb * 2);
+        dmax = std::max(dmax, rows * size_t(dbytes_per_row(int64_t(ms[i].nb) * kQK, fmt)));
         nb_max = std::max(nb_max, ms[i].nb);
     }
     pl.nb_max = nb_max;
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
-    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T) + size_t(2 * kCW * 32) * 4 +
+    pl.dstage = fmt == 2 ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
+    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * kCW * 32) * 4 +
                          size_t(kCW * 32) * 12;
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
-    const size_t per = size_t(pl.cstage) + pl.sstage;
+    const size_t per = size_t(pl.cstage) + pl.sstage + pl.dstage;
     const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
     int ns = int(std::min(kRingBudget, room) / per);
     ns = std::min(ns, 32);
@@ -701,6 +838,7 @@ static cudaError_t launch_gemv(GemvParams<MAXM>& prm, const Plan& pl, int grid, 
 {
     prm.cstage = pl.cstage;
     prm.sstage = pl.sstage;
+    prm.dstage = pl.dstage;
     prm.nst = pl.ns;
     prm.nb_max = pl.nb_max;
     prm.pf = kPrefetchStages;
@@ -764,6 +902,7 @@ static cudaError_t single_f(const GemvMat& m, int T, float* cv, int* ci, cudaStr
 static cudaError_t single(const GemvMat& m, int fmt, int T, bool head, float* cv, int* ci, cudaStream_t s, int* g)
 {
     if (fmt == 0) return head ? single_f<0, true>(m, T, cv, ci, s, g) : single_f<0, false>(m, T, cv, ci, s, g);
+    if (fmt == 2) return head ? single_f<2, true>(m, T, cv, ci, s, g) : single_f<2, false>(m, T, cv, ci, s, g);
     return head ? single_f<1, true>(m, T, cv, ci, s, g) : single_f<1, false>(m, T, cv, ci, s, g);
 }
 
@@ -788,7 +927,7 @@ static cudaError_t grouped_t(const strata_gemv_desc* d, int n, cudaStream_t stre
     for (int i = 0; i < n; ++i) {
         prm.m[i] = make_mat(d[i].W, d[i].rows, d[i].cols, FMT, d[i].xq, d[i].xd, d[i].xs, d[i].y, chunks);
         const int nc = int((d[i].rows + kR - 1) / kR);
-        const double cb = double(kR) * (d[i].cols / kQK) * (qbytes_of(FMT) + 2);
+        const double cb = double(kR) * ((d[i].cols / kQK) * (qbytes_of(FMT) + 2) + dbytes_per_row(d[i].cols, FMT));
         for (int c = 0; c < nc; ++c) cum.push_back(cum.back() + cb);
         chunks += nc;
     }
@@ -824,6 +963,7 @@ static cudaError_t grouped_f(const strata_gemv_desc* d, int n, int T, cudaStream
 
 cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T, cudaStream_t stream)
 {
+    if (fmt == 2) return grouped_f<2>(d, n, T, stream);
     return fmt == 0 ? grouped_f<0>(d, n, T, stream) : grouped_f<1>(d, n, T, stream);
 }
 
@@ -878,6 +1018,8 @@ cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt
     const uint8_t* w = static_cast<const uint8_t*>(W);
     if (fmt == 0)
         return launch_pdl(block_dots_kernel<0>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
+    if (fmt == 2)
+        return launch_pdl(block_dots_kernel<2>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
     return launch_pdl(block_dots_kernel<1>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
 }
 

@@ -39,6 +39,15 @@
  *   index r*nb + b. Total bytes = rows*nb*18 (Q4) or rows*nb*34 (Q8), the same as interleaved
  *   {half d; codes} blocks, but both planes start on 16-byte boundaries so that every block's
  *   codes are one or two aligned 16-byte loads. W must be 16-byte aligned.
+ *     STRATA_Q6 (the pages' 6-bit super-block type, 210 bytes per 256 weights; cols % 256 == 0):
+ *                code plane rows*nb*24 bytes, block (r, b) at (r*nb + b)*24: bytes 0..15 hold the low
+ *                4 bits of element j (low nibble) and of element j+16 (high nibble); byte 16+i
+ *                (i < 8) holds the high 2 bits of elements i, i+8, i+16, i+24 in bits 0-1, 2-3, 4-5,
+ *                6-7; the code q = low | high << 4 is in 0..63. Then rows*nb*2 bytes of int8
+ *                sub-scales (s0, s1 of block (r, b) at 2*(r*nb + b): s0 for elements 0..15, s1 for
+ *                16..31), then rows*(cols/256) fp16 super-block scales d (row r, super-block k at
+ *                index r*(cols/256) + k). The weight is w = d * s * (q - 32); the integer dot is
+ *                exact per 16 weights and each 16 contributes its own term d * s * d_x * isum16.
  *
  * Quantized activations (q8_1-style, one scale and one sum per 32 values), for n rows of `cols`:
  *     xq int8  [n][cols]   codes q in -127..127
@@ -78,7 +87,7 @@ extern "C" {
 
 #define STRATA_MAX_T 8             /* verify windows hold 1..8 tokens */
 
-typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1 } strata_fmt;
+typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1, STRATA_Q6 = 2 } strata_fmt;
 
 /* Static text for a status code (never NULL). */
 const char* strata_error_string(int status);
