@@ -411,10 +411,11 @@ def main():
            "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(T * 4)}
 
     # --- prompt-chunk MoE (grouped experts), reported beside the window ---
-    moe = gemm = None
+    moe = gemm = q6 = None
     if not args.no_moe:
         moe = bench_moe(torch, strata, synth, args)
         gemm = bench_prompt_gemm(torch, strata, synth)
+        q6 = bench_q6_layers(torch, strata, synth, hbm_peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -437,11 +438,42 @@ def main():
             "per_T": per_T, "chained_launches": chained, "batch_head_margin": hb, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe, "prompt_gemm": gemm,
+            "q6_layers": q6,
             "device_error_word": strata.device_error(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def bench_q6_layers(torch, strata, synth, hbm_peak, layers=16, reps=20):
+    """The window's layer projections in the Q6 super-block format (one grouped launch per window;
+    16 layers, 0.58 GB of weights, larger than L2) at T = 2 and 4: weight GB/s and HBM fraction."""
+    from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
+    wts = WindowWeights(layers=layers, device="cuda", key="q6-window", layer_fmt=synth.Q6)
+    lay_bytes = sum(synth.weight_nbytes(r, c, f) for _, r, c, f in wts.shapes[:-1])
+    out = {"workload": f"{layers} layers x {{qkv 2048->5120, o 4096->2048, up 2048->6144, down 6144->2048}} Q6",
+           "weight_bytes": lay_bytes}
+    for T in (2, 4):
+        win = VerifyWindow(wts, T)
+        win.load_inputs()
+        g = win.capture("layers")
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        gbs = lay_bytes / (ms * 1e-3) / 1e9
+        out[f"T{T}"] = {"us": ms * 1e3, "weight_gbs": gbs, "hbm_frac": gbs / hbm_peak}
+        del g, win
+    del wts
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_prompt_gemm(torch, strata, synth, reps=20):
@@ -552,7 +584,7 @@ def run_case(args):
         return
     if args.case == "layers":  # the window's grouped layer launch (quantize per width + one GEMV launch)
         from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
-        wts = WindowWeights(layers=args.layers, device="cuda")
+        wts = WindowWeights(layers=args.layers, device="cuda", layer_fmt=args.fmt)
         win = VerifyWindow(wts, T)
         win.load_inputs()
         g = win.capture("layers")
@@ -567,7 +599,7 @@ def run_case(args):
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / args.reps
         nbytes = wts.weight_bytes - synth.weight_nbytes(synth.HEAD_VOCAB, synth.WINDOW_HIDDEN, synth.Q8)
-        print(json.dumps({"case": "layers", "layers": args.layers, "T": T, "us": ms * 1e3,
+        print(json.dumps({"case": "layers", "layers": args.layers, "fmt": args.fmt, "T": T, "us": ms * 1e3,
                           "weight_gbs": nbytes / (ms * 1e-3) / 1e9, "device_error": strata.device_error()}))
         return
     if args.case in ("mmvq", "head"):

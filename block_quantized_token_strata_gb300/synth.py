@@ -146,12 +146,13 @@ WINDOW_PROJ = (("qkv", 5120, 2048), ("o", 2048, 4096), ("up", 6144, 2048), ("dow
 HEAD_VOCAB = 151936
 
 
-def window_shapes(layers: int = WINDOW_LAYERS):
-    """[(name, rows, cols, fmt)] of every matrix of the verify window, in launch order."""
+def window_shapes(layers: int = WINDOW_LAYERS, layer_fmt: int = Q4):
+    """[(name, rows, cols, fmt)] of every matrix of the verify window, in launch order (the layer
+    projections in ``layer_fmt``, Q4 by default; the head in Q8)."""
     out = []
     for layer in range(layers):
         for name, rows, cols in WINDOW_PROJ:
-            out.append((f"L{layer}.{name}", rows, cols, Q4))
+            out.append((f"L{layer}.{name}", rows, cols, layer_fmt))
     out.append(("head", HEAD_VOCAB, WINDOW_HIDDEN, Q8))
     return out
 

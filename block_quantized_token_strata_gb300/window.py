@@ -24,8 +24,10 @@ from . import strata, synth
 class WindowWeights:
     """Device copies of every matrix of the window (generated once, seeded)."""
 
-    def __init__(self, layers: int = synth.WINDOW_LAYERS, device="cuda", key="window", host_copy=False):
-        self.shapes = synth.window_shapes(layers)
+    def __init__(self, layers: int = synth.WINDOW_LAYERS, device="cuda", key="window", host_copy=False,
+                 layer_fmt: int = synth.Q4):
+        self.layer_fmt = layer_fmt
+        self.shapes = synth.window_shapes(layers, layer_fmt)
         self.dev = []
         self.host = [] if host_copy else None
         for name, rows, cols, fmt in self.shapes:
@@ -110,7 +112,7 @@ class VerifyWindow:
             if part in ("all", "layers"):
                 for c in self.widths:
                     strata.quantize_act(self.gx[c], self.gq[c], self.gd[c], self.gs[c], stream=stream)
-                strata.mmvq_grouped(self.descs, synth.Q4, self.T, stream=stream)
+                strata.mmvq_grouped(self.descs, self.wts.layer_fmt, self.T, stream=stream)
         else:
             if part in ("all", "layers"):
                 for i in range(n - 1):
