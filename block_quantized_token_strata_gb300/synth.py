@@ -11,6 +11,8 @@ Distributions (the workload recipe):
   * Q8 codes q ~ U{-127..127};
   * Q6 (256-weight super-blocks): codes q ~ U{0..63}, sub-block scales ~ U{-127..127} (int8, one
     per 16 weights), super-block scale d = fp16(|N(0,1)| * 0.001);
+  * Q4K (256-weight super-blocks with minimums): codes q ~ U{0..15}, per 32 weights a scale
+    sc ~ U{0..63} and a minimum m ~ U{0..63}, per 256 weights d and dmin = fp16(|N(0,1)| * 0.001);
   * activations x ~ N(0,1) fp32, optionally with a Bernoulli(0.01) mask of elements scaled x20;
   * MoE routing: k distinct experts per token drawn without replacement from a Zipf(1.1)
     law over expert ranks, p_e proportional to (e+1)^-1.1, draw order = slot order.
@@ -23,8 +25,8 @@ import numpy as np
 
 QK = 32
 QKS = 256  # Q6 super-block
-Q4, Q8, Q6 = 0, 1, 2
-_QBYTES = {Q4: 16, Q8: 32, Q6: 24}
+Q4, Q8, Q6, Q4K = 0, 1, 2, 3
+_QBYTES = {Q4: 16, Q8: 32, Q6: 24, Q4K: 16}
 
 
 def _rng(*key) -> np.random.Generator:
@@ -40,7 +42,8 @@ def _rng(*key) -> np.random.Generator:
 
 def weight_nbytes(rows: int, cols: int, fmt: int) -> int:
     nb = rows * (cols // QK)
-    extra = rows * (cols // QKS) * 2 if fmt == Q6 else 0   # Q6: one fp16 d per super-block
+    # per super-block: Q6 one fp16 d, Q4K fp16 d and dmin
+    extra = rows * (cols // QKS) * (2 if fmt == Q6 else 4) if fmt in (Q6, Q4K) else 0
     return nb * (_QBYTES[fmt] + 2) + extra
 
 
@@ -89,6 +92,18 @@ def make_q6_buffer(q: np.ndarray, sub: np.ndarray, d: np.ndarray) -> np.ndarray:
                            np.asarray(d, np.float16).reshape(-1).view(np.uint8)])
 
 
+def make_q4k_buffer(q: np.ndarray, sc: np.ndarray, mn: np.ndarray, d: np.ndarray, dmin: np.ndarray) -> np.ndarray:
+    """Lay out Q4K codes q uint8 [rows][cols] (0..15), per-32 scales sc and minimums mn uint8
+    [rows][cols/32] (0..63) and per-256 fp16 d, dmin [rows][cols/256] in the planar Q4K format."""
+    rows, cols = q.shape
+    nb = cols // QK
+    qb = q.reshape(rows, nb, 32).astype(np.uint8)
+    code = (qb[:, :, :16] & 15) | ((qb[:, :, 16:] & 15) << 4)
+    smp = np.stack([np.asarray(sc, np.uint8), np.asarray(mn, np.uint8)], axis=-1)
+    dd = np.stack([np.asarray(d, np.float16), np.asarray(dmin, np.float16)], axis=-1)
+    return np.concatenate([code.reshape(-1), smp.reshape(-1), dd.reshape(-1).view(np.uint8)])
+
+
 def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
     """A seeded [rows][cols] matrix in Q4, Q8 or Q6 (planar layout, see include/strata.h)."""
     if cols % QK or rows <= 0:
@@ -101,6 +116,15 @@ def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
         sub = rng.integers(-127, 128, size=(rows, cols // 16), dtype=np.int8)
         d = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
         return Weights(rows, cols, fmt, make_q6_buffer(q, sub, d))
+    if fmt == Q4K:
+        if cols % QKS:
+            raise ValueError("Q4K needs cols % 256 == 0")
+        q = rng.integers(0, 16, size=(rows, cols), dtype=np.uint8)
+        sc = rng.integers(0, 64, size=(rows, cols // QK), dtype=np.uint8)
+        mn = rng.integers(0, 64, size=(rows, cols // QK), dtype=np.uint8)
+        d = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
+        dmin = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
+        return Weights(rows, cols, fmt, make_q4k_buffer(q, sc, mn, d, dmin))
     nb = rows * (cols // QK)
     d = (np.abs(rng.standard_normal(nb)) * 0.01).astype(np.float16)
     if fmt == Q4:

@@ -19,7 +19,10 @@
  *   Q4 block = fp16 d + 32 unsigned 4-bit codes, w = d*(q-8); Q8 block = fp16 d + 32 int8 codes,
  *   w = d*q; Q6 (the pages' 6-bit super-block type, 210 bytes per 256 weights): per 256 weights an
  *   fp16 d, per 16 weights an int8 sub-scale s, 6-bit codes q, w = d*s*(q-32), with exact integer
- *   dots per 16 weights (one term per sub-scale); activations: per 32 values amax, d = amax/127 (fp32), q = roundf(x/d) via x*(1/d),
+ *   dots per 16 weights (one term per sub-scale); Q4K (the pages' 4-bit super-block type with
+ *   minimums): per 32 weights a 6-bit scale sc and minimum m, per 256 weights fp16 d and dmin, 4-bit
+ *   codes q, w = d*sc*q - dmin*m, two terms per 32 weights (d*sc*d_x*isum and -dmin*m*d_x*sum x);
+ *   activations: per 32 values amax, d = amax/127 (fp32), q = roundf(x/d) via x*(1/d),
  *   s = sum q; MoE hidden h = silu(g)*u with silu(g) = g/(1+exp(-g)), re-quantized the same way.
  *
  * Arithmetic: integer dots in int64 (exact); block terms d_w * d_x * isum and all sums in fp64, in
@@ -37,6 +40,7 @@
 #define OR_Q4 0
 #define OR_Q8 1
 #define OR_Q6 2
+#define OR_Q4K 3
 
 /* ---- IEEE 754 binary16 -> double, from the format's definition ---------------------------- */
 double or_half_to_double(uint16_t h)
@@ -56,7 +60,7 @@ double or_half_to_double(uint16_t h)
 }
 
 /* ---- the planar weight layout ---------------------------------------------------------------- */
-static int64_t qbytes(int fmt) { return fmt == OR_Q4 ? 16 : (fmt == OR_Q8 ? 32 : 24); }
+static int64_t qbytes(int fmt) { return (fmt == OR_Q4 || fmt == OR_Q4K) ? 16 : (fmt == OR_Q8 ? 32 : 24); }
 
 /* Q4/Q8: the fp16 scale of block (r, b). Q6: the fp16 d of the super-block holding block b, which
  * sits after the code plane (24 bytes a block) and the sub-scale plane (2 int8 a block). */
@@ -65,10 +69,23 @@ static double block_scale(const uint8_t* W, int64_t rows, int64_t nb, int fmt, i
     const uint8_t* p;
     if (fmt == OR_Q6)
         p = W + rows * nb * 26 + 2 * (r * (nb / 8) + b / 8);
+    else if (fmt == OR_Q4K)  /* d of the super-block (dmin follows it) */
+        p = W + rows * nb * 18 + 4 * (r * (nb / 8) + b / 8);
     else
         p = W + rows * nb * qbytes(fmt) + 2 * (r * nb + b);
     uint16_t bits = (uint16_t)(p[0] | (p[1] << 8));
     return or_half_to_double(bits);
+}
+
+/* Q4K: the super-block's fp16 dmin, and block (r, b)'s 6-bit scale (k = 0) or minimum (k = 1) */
+static double q4k_dmin(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, int64_t b)
+{
+    const uint8_t* p = W + rows * nb * 18 + 4 * (r * (nb / 8) + b / 8) + 2;
+    return or_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
+}
+static int q4k_scale_min(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, int64_t b, int k)
+{
+    return (int)W[rows * nb * 16 + 2 * (r * nb + b) + k];
 }
 
 /* Q6: the int8 sub-scale of half h (elements 16h..16h+15) of block (r, b) */
@@ -81,10 +98,10 @@ static int q6_subscale(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, in
 static int weight_code(const uint8_t* W, int64_t nb, int fmt, int64_t r, int64_t b, int j)
 {
     const uint8_t* blk = W + (r * nb + b) * qbytes(fmt);
-    if (fmt == OR_Q4) {
+    if (fmt == OR_Q4 || fmt == OR_Q4K) {  /* Q4K codes carry no offset: its minimum does that */
         int byte = blk[j & 15];
         int q = (j < 16) ? (byte & 0x0F) : (byte >> 4);
-        return q - 8;
+        return fmt == OR_Q4 ? q - 8 : q;
     }
     if (fmt == OR_Q6) {
         /* bytes 0..15: low 4 bits of element j (low nibble) and of element j+16 (high nibble);
@@ -162,6 +179,18 @@ static void row_dot(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t
 {
     double acc = 0.0, aabs = 0.0;
     for (int64_t b = 0; b < nb; ++b) {
+        if (fmt == OR_Q4K) {  /* d*sc*d_x*isum, then -dmin*m*d_x*(sum of the block's x codes) */
+            int64_t isum = block_isum(W, rows, nb, fmt, r, b, xq_row + 32 * b), xsum = 0;
+            for (int j = 0; j < 32; ++j) xsum += xq_row[32 * b + j];
+            double t1 = block_scale(W, rows, nb, fmt, r, b) * (double)q4k_scale_min(W, rows, nb, r, b, 0) *
+                        (double)xd_row[b] * (double)isum;
+            double t2 = -q4k_dmin(W, rows, nb, r, b) * (double)q4k_scale_min(W, rows, nb, r, b, 1) *
+                        (double)xd_row[b] * (double)xsum;
+            acc += t1;
+            acc += t2;
+            aabs += fabs(t1) + fabs(t2);
+            continue;
+        }
         if (fmt == OR_Q6) {  /* one term per 16 weights: d * s_h * d_x * isum_h */
             for (int h = 0; h < 2; ++h) {
                 int64_t isum = half_isum(W, nb, fmt, r, b, xq_row + 32 * b, h);

@@ -360,3 +360,59 @@ def test_q6_brute_force_dense(orc):
     # the generator's buffer decodes the same way
     from block_quantized_token_strata_gb300 import synth
     assert np.array_equal(synth.make_q6_buffer(q, sub, d), W)
+
+
+# ---- Q4K (4-bit codes, 6-bit scale and minimum per 32 weights, fp16 d and dmin per 256) --------------
+def pack_q4k(q, sc, mn, d, dmin) -> np.ndarray:
+    """This test's own packer: Q4 code bytes (no offset), then (sc, m) byte pairs per block, then
+    (d, dmin) fp16 pairs per super-block."""
+    rows, cols = q.shape
+    out = bytearray()
+    for r in range(rows):
+        for b in range(cols // 32):
+            blk = [int(v) for v in q[r, 32 * b:32 * b + 32]]
+            out += bytes(blk[j] | (blk[j + 16] << 4) for j in range(16))
+    for r in range(rows):
+        for b in range(cols // 32):
+            out += bytes([int(sc[r, b]), int(mn[r, b])])
+    for r in range(rows):
+        for k in range(cols // 256):
+            out += np.array([d[r, k], dmin[r, k]], np.float16).tobytes()
+    return np.frombuffer(bytes(out), np.uint8).copy()
+
+
+def test_q4k_one_superblock_by_hand(orc):
+    """cols = 256, x codes all 1 with d_x = 1 (block sums 32), d = dmin = 1: codes 15 with sc 1 and
+    m 0 give 8 blocks x 32 x 15 = 3840; adding m = 2 subtracts 8 x 2 x 32 = 512; sc 0 and m 1 give
+    -8 x 32 = -256."""
+    xq = np.ones((1, 256), np.int8)
+    xd = np.ones((1, 8), np.float32)
+    one = np.ones((1, 1), np.float16)
+    for code, sc, mn, want in [(15, 1, 0, 3840.0), (15, 1, 2, 3328.0), (7, 0, 1, -256.0), (0, 63, 0, 0.0)]:
+        W = pack_q4k(np.full((1, 256), code, np.uint8), np.full((1, 8), sc), np.full((1, 8), mn), one, one)
+        y, A = orc.mmvq(W, 1, 256, 3, xq, xd)
+        assert y[0, 0] == want, (code, sc, mn, y)
+
+
+def test_q4k_brute_force_dense(orc):
+    rng = np.random.default_rng(23)
+    rows, cols, T = 7, 512, 3
+    q = rng.integers(0, 16, size=(rows, cols)).astype(np.uint8)
+    sc = rng.integers(0, 64, size=(rows, cols // 32)).astype(np.uint8)
+    mn = rng.integers(0, 64, size=(rows, cols // 32)).astype(np.uint8)
+    d = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+    dmin = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+    W = pack_q4k(q, sc, mn, d, dmin)
+    assert W.size == rows * (cols // 256) * 148
+    xq, xd, _ = orc.quantize_act(rng.standard_normal((T, cols)).astype(np.float32))
+    w = (d.astype(np.float64).repeat(256, axis=1) * sc.astype(np.float64).repeat(32, axis=1) * q
+         - dmin.astype(np.float64).repeat(256, axis=1) * mn.astype(np.float64).repeat(32, axis=1))
+    ref = (xq.astype(np.float64) * xd.astype(np.float64).repeat(32, axis=1)) @ w.T
+    y, A = orc.mmvq(W, rows, cols, 3, xq, xd)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # block dots are the unscaled sums of q * x
+    isum = orc.block_dots(W, rows, cols, 3, xq)
+    want = np.einsum("rbj,tbj->trb", q.astype(np.int64).reshape(rows, -1, 32), xq.astype(np.int64).reshape(T, -1, 32))
+    assert np.array_equal(isum.reshape(T, rows, cols // 32), want)
+    from block_quantized_token_strata_gb300 import synth
+    assert np.array_equal(synth.make_q4k_buffer(q, sc, mn, d, dmin), W)
