@@ -83,6 +83,11 @@ template <> struct FmtInfo<1> { static constexpr int kQB = 32; };  // Q8: 32 cod
 // Q6: 24 code bytes per block (16 of low 4-bit parts, 8 of high 2-bit parts); its "scale plane" holds
 // the two int8 sub-scales of each block, and a third plane one fp16 d per 8 blocks (256 weights)
 template <> struct FmtInfo<2> { static constexpr int kQB = 24; };
+// Q4K: Q4's 16 code bytes (codes 0..15, no offset); its "scale plane" holds each block's 6-bit scale
+// and minimum, the third plane fp16 d and dmin per 8 blocks
+template <> struct FmtInfo<3> { static constexpr int kQB = 16; };
+// bytes per super-block (256 weights) in the third plane
+template <int FMT> struct SuperInfo { static constexpr int kDB = FMT == 2 ? 2 : (FMT == 3 ? 4 : 0); };
 
 struct GemvMat {
     const uint8_t* W;
@@ -285,10 +290,11 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 const uintptr_t sa = reinterpret_cast<uintptr_t>(m.W + size_t(m.rows) * m.nb * QB + size_t(r0) * m.nb * 2);
                 const uintptr_t lo = (sa + 15) & ~uintptr_t(15), hi2 = (sa + uint32_t(nr) * m.nb * 2) & ~uintptr_t(15);
                 if (hi2 > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), uint32_t(hi2 - lo));
-                if constexpr (FMT == 2) {
+                if constexpr (SuperInfo<FMT>::kDB > 0) {
+                    constexpr int DB = SuperInfo<FMT>::kDB;
                     const uintptr_t da = reinterpret_cast<uintptr_t>(m.W + size_t(m.rows) * m.nb * (QB + 2) +
-                                                                     size_t(r0) * (m.nb / 8) * 2);
-                    const uintptr_t dlo = (da + 15) & ~uintptr_t(15), dhi = (da + uint32_t(nr) * (m.nb / 8) * 2) & ~uintptr_t(15);
+                                                                     size_t(r0) * (m.nb / 8) * DB);
+                    const uintptr_t dlo = (da + 15) & ~uintptr_t(15), dhi = (da + uint32_t(nr) * (m.nb / 8) * DB) & ~uintptr_t(15);
                     if (dhi > dlo) bulk_prefetch_l2(reinterpret_cast<const void*>(dlo), uint32_t(dhi - dlo));
                 }
                 pf.next();
@@ -329,10 +335,11 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 const uint8_t* dsrc = nullptr;
                 uint8_t* ddst = nullptr;
                 uint32_t dhead = 0, dmid = 0;
-                if constexpr (FMT == 2) {
+                if constexpr (SuperInfo<FMT>::kDB > 0) {
+                    constexpr int DB = SuperInfo<FMT>::kDB;
                     const int ns = m.nb / 8;
-                    dsrc = m.W + size_t(m.rows) * m.nb * (QB + 2) + size_t(r0) * ns * 2;
-                    const uint32_t dbytes = uint32_t(nr) * ns * 2;
+                    dsrc = m.W + size_t(m.rows) * m.nb * (QB + 2) + size_t(r0) * ns * DB;
+                    const uint32_t dbytes = uint32_t(nr) * ns * DB;
                     const uint32_t dmis = uint32_t(reinterpret_cast<uintptr_t>(dsrc) & 15);
                     ddst = dring + s * p.dstage + dmis;
                     dhead = min(dbytes, (16u - dmis) & 15u);
@@ -396,10 +403,11 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
             for (int i = threadIdx.x; i < nb * TPP; i += kCW * 32) {
                 const int b = i / TPP, t = i - (i / TPP) * TPP;
                 float d = 0.0f;
-                int c0 = kMagicBits, c1 = kMagicBits;
+                int c0 = (FMT == 3) ? 0 : kMagicBits, c1 = kMagicBits;  // Q4K: the block sum as a float
                 if (t < T) {
                     d = __ldg(m.xd + t * nb + b);
                     if (FMT == 0) c0 = kMagicBits - 8 * __ldg(m.xs + t * nb + b);
+                    if (FMT == 3) c0 = __float_as_int(float(__ldg(m.xs + t * nb + b)));  // exact: |s| <= 4064
                     if (FMT == 2) {
                         // Q6 codes stand for q - 32 and carry one sub-scale per 16: seed each half's chain
                         // with -32 times that half's activation sum
@@ -523,6 +531,63 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                                     const f32x2 fh = add_f2(pack_f2(__int_as_float(ha), __int_as_float(hb)), negm);
                                     acc[r][q] = fma_f2(mul_f2(sdl2[r], dx2), fl, acc[r][q]);
                                     acc[r][q] = fma_f2(mul_f2(sdh2[r], dx2), fh, acc[r][q]);
+                                }
+                            }
+                        }
+                    } else if constexpr (FMT == 3) {
+                        // Q4K: per block 16 code bytes (codes 0..15), a 6-bit scale and minimum; per 8
+                        // blocks fp16 d and dmin. Terms: (d*sc*d_x)*isum, then (-dmin*m*d_x)*sum(x)
+                        const uintptr_t dsrc = reinterpret_cast<uintptr_t>(m.W + size_t(rows) * nb * (QB + 2) +
+                                                                           size_t(r0s) * (nb / 8) * 4);
+                        const unsigned short* dpl = reinterpret_cast<const unsigned short*>(
+                            dring + s * p.dstage + int(dsrc & 15) + pos * (kR * 4) * (nb / 8));
+                        const int ns = nb / 8;
+                        for (int kb = gl; kb < nb; kb += G) {
+                            const uint8_t* wp = cb + kb * QB;
+                            const unsigned short* sp = sc + kb;
+                            const uint8_t* xr = xsm + kb * RX;
+                            uint4 w[kR];
+                            f32x2 sc2[kR], mn2[kR];
+#pragma unroll
+                            for (int r = 0; r < kR; ++r) {
+                                w[r] = *reinterpret_cast<const uint4*>(wp + r * rsw);
+                                const unsigned short su = sp[r * nb];
+                                const int di = 2 * (r * ns + (kb >> 3));
+                                const float dd = __half2float(__ushort_as_half(dpl[di]));
+                                const float dm = __half2float(__ushort_as_half(dpl[di + 1]));
+                                // d * sc and dmin * m are exact in fp32 (11 + 6 significant bits)
+                                const float sv = __fmul_rn(dd, float(su & 0xFF));
+                                const float mv = __fmul_rn(dm, float(su >> 8));
+                                sc2[r] = pack_f2(sv, sv);
+                                mn2[r] = pack_f2(-mv, -mv);
+                            }
+                            float dxv[TPP], xsv[TPP];
+#pragma unroll
+                            for (int q = 0; q < TPP; q += 2) {
+                                const float2 dd = *reinterpret_cast<const float2*>(xr + T * 32 + q * 4);
+                                const float2 ss = *reinterpret_cast<const float2*>(xr + T * 32 + TPP * 4 + q * 4);
+                                dxv[q] = dd.x; dxv[q + 1] = dd.y;
+                                xsv[q] = ss.x; xsv[q + 1] = ss.y;
+                            }
+#pragma unroll
+                            for (int q = 0; q < NP; ++q) {
+                                const int ta = 2 * q, tb = 2 * q + 1;
+                                const uint4 xla = *reinterpret_cast<const uint4*>(xr + ta * 32);
+                                const uint4 xha = *reinterpret_cast<const uint4*>(xr + ta * 32 + 16);
+                                uint4 xlb = xla, xhb = xha;
+                                if (tb < T) {
+                                    xlb = *reinterpret_cast<const uint4*>(xr + tb * 32);
+                                    xhb = *reinterpret_cast<const uint4*>(xr + tb * 32 + 16);
+                                }
+                                const f32x2 dx2 = pack_f2(dxv[ta], dxv[tb]);
+                                const f32x2 xs2 = pack_f2(xsv[ta], xsv[tb]);
+#pragma unroll
+                                for (int r = 0; r < kR; ++r) {
+                                    const int ca = dot_q4(w[r], xla, xha, kMagicBits);
+                                    const int cbv = (tb < T) ? dot_q4(w[r], xlb, xhb, kMagicBits) : kMagicBits;
+                                    const f32x2 f2 = add_f2(pack_f2(__int_as_float(ca), __int_as_float(cbv)), negm);
+                                    acc[r][q] = fma_f2(mul_f2(sc2[r], dx2), f2, acc[r][q]);
+                                    acc[r][q] = fma_f2(mul_f2(mn2[r], dx2), xs2, acc[r][q]);
                                 }
                             }
                         }
@@ -731,7 +796,7 @@ __global__ void __launch_bounds__(256) block_dots_kernel(const uint8_t* __restri
         const uint4* xp = reinterpret_cast<const uint4*>(xq + size_t(t) * nb * 32 + size_t(b) * 32);
         const uint4 xl = xp[0], xh = xp[1];
         const int c0 = (FMT == 0) ? kMagicBits - 8 * xs[size_t(t) * nb + b] : kMagicBits;
-        const int c = (FMT == 0) ? dot_q4(w0, xl, xh, c0) : dot_q8(w0, w1, xl, xh, c0);
+        const int c = (FMT == 0 || FMT == 3) ? dot_q4(w0, xl, xh, c0) : dot_q8(w0, w1, xl, xh, c0);
         isum[(size_t(t) * rows + r) * nb + b] = c - kMagicBits;
     }
 }
@@ -751,9 +816,9 @@ int device_sm_count()
     return cache[dev];
 }
 
-static int qbytes_of(int fmt) { return fmt == 0 ? 16 : (fmt == 1 ? 32 : 24); }
+static int qbytes_of(int fmt) { return (fmt == 0 || fmt == 3) ? 16 : (fmt == 1 ? 32 : 24); }
 // weight bytes per row group beyond the codes and the per-block 2-byte plane: Q6's super-block d
-static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : 0; }
+static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : (fmt == 3 ? (cols / 256) * 4 : 0); }
 
 // Warps per row: a function of (cols, fmt) only, so every launch of a shape (any T, single or
 // grouped) sums each row in the same order. As few warps as keep at least two blocks per lane
@@ -808,7 +873,7 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     pl.nb_max = nb_max;
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
-    pl.dstage = fmt == 2 ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
+    pl.dstage = (fmt == 2 || fmt == 3) ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
     const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * kCW * 32) * 4 +
                          size_t(kCW * 32) * 12;
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
@@ -903,6 +968,7 @@ static cudaError_t single(const GemvMat& m, int fmt, int T, bool head, float* cv
 {
     if (fmt == 0) return head ? single_f<0, true>(m, T, cv, ci, s, g) : single_f<0, false>(m, T, cv, ci, s, g);
     if (fmt == 2) return head ? single_f<2, true>(m, T, cv, ci, s, g) : single_f<2, false>(m, T, cv, ci, s, g);
+    if (fmt == 3) return head ? single_f<3, true>(m, T, cv, ci, s, g) : single_f<3, false>(m, T, cv, ci, s, g);
     return head ? single_f<1, true>(m, T, cv, ci, s, g) : single_f<1, false>(m, T, cv, ci, s, g);
 }
 
@@ -964,6 +1030,7 @@ static cudaError_t grouped_f(const strata_gemv_desc* d, int n, int T, cudaStream
 cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T, cudaStream_t stream)
 {
     if (fmt == 2) return grouped_f<2>(d, n, T, stream);
+    if (fmt == 3) return grouped_f<3>(d, n, T, stream);
     return fmt == 0 ? grouped_f<0>(d, n, T, stream) : grouped_f<1>(d, n, T, stream);
 }
 
@@ -1018,6 +1085,8 @@ cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt
     const uint8_t* w = static_cast<const uint8_t*>(W);
     if (fmt == 0)
         return launch_pdl(block_dots_kernel<0>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
+    if (fmt == 3)
+        return launch_pdl(block_dots_kernel<3>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
     if (fmt == 2)
         return launch_pdl(block_dots_kernel<2>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
     return launch_pdl(block_dots_kernel<1>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);

@@ -48,6 +48,14 @@
  *                16..31), then rows*(cols/256) fp16 super-block scales d (row r, super-block k at
  *                index r*(cols/256) + k). The weight is w = d * s * (q - 32); the integer dot is
  *                exact per 16 weights and each 16 contributes its own term d * s * d_x * isum16.
+ *     STRATA_Q4K (the pages' 4-bit super-block type with minimums, 148 bytes per 256 weights;
+ *                cols % 256 == 0): the Q4 code plane (16 bytes a block, codes q in 0..15 with no
+ *                offset), then rows*nb byte pairs (sc, m) per block (6-bit scale and minimum, 0..63),
+ *                then rows*(cols/256) pairs of fp16 (d, dmin) per super-block. The weight is
+ *                w = d * sc * q - dmin * m; each block contributes d*sc*d_x*isum then
+ *                -dmin*m*d_x*s, with isum = sum q*x exact and s the activation block sum.
+ *   The block-dot hook (strata_block_dots) returns isum as defined per format: Q4 sum (q-8)x, Q8
+ *   sum qx, Q6 s0*sum16 + s1*sum16, Q4K sum qx.
  *
  * Quantized activations (q8_1-style, one scale and one sum per 32 values), for n rows of `cols`:
  *     xq int8  [n][cols]   codes q in -127..127
@@ -87,7 +95,7 @@ extern "C" {
 
 #define STRATA_MAX_T 8             /* verify windows hold 1..8 tokens */
 
-typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1, STRATA_Q6 = 2 } strata_fmt;
+typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1, STRATA_Q6 = 2, STRATA_Q4K = 3 } strata_fmt;
 
 /* Static text for a status code (never NULL). */
 const char* strata_error_string(int status);

@@ -1,7 +1,8 @@
-"""GPU parity of the Q6 super-block format (6-bit codes, int8 sub-scale per 16 weights, fp16 d per 256)
-through the same GEMV family: exact integer dots (bit for bit), outputs within the fp32 bound of
-the oracle, every column of a T-token launch bitwise equal to the T = 1 launch, grouped launches
-equal to single calls.
+"""GPU parity of the 256-weight super-block formats through the same GEMV family: Q6 (6-bit codes,
+int8 sub-scale per 16 weights, fp16 d per 256) and Q4K (4-bit codes, 6-bit scale and minimum per 32
+weights, fp16 d and dmin per 256). Bars: exact integer dots (bit for bit), outputs within the fp32
+bound of the oracle, every column of a T-token launch bitwise equal to the T = 1 launch, grouped
+launches equal to single calls.
 """
 import numpy as np
 import pytest
@@ -11,7 +12,7 @@ import oracle
 from block_quantized_token_strata_gb300 import strata, synth
 
 pytestmark = pytest.mark.gpu
-Q6 = synth.Q6
+FMTS = [synth.Q6, synth.Q4K]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,7 +33,8 @@ def assert_within(y_gpu, y_or, A, what=""):
     assert not (err > tol).any(), f"{what}: {(err > tol).sum()} outside the bound"
 
 
-def test_q6_block_dots_exact():
+@pytest.mark.parametrize("Q6", FMTS)
+def test_q6_block_dots_exact(Q6):
     rows, cols, T = 37, 768, 3
     w = synth.make_weights(rows, cols, Q6, "q6dots")
     x = synth.make_activations(T, cols, "q6dots", outliers=True)
@@ -50,7 +52,8 @@ def test_q6_block_dots_exact():
     (10240, 2560, 2, False),    # the pages' Q6 MMVQ shape at T = 2
     (1, 256, 8, False),         # one row, one super-block
 ])
-def test_q6_mmvq_matches_oracle(rows, cols, T, outl):
+@pytest.mark.parametrize("Q6", FMTS)
+def test_q6_mmvq_matches_oracle(Q6, rows, cols, T, outl):
     w = synth.make_weights(rows, cols, Q6, "q6mmvq")
     x = synth.make_activations(T, cols, "q6mmvq", outliers=outl)
     xq, xd, xs = oracle.quantize_act(x)
@@ -65,7 +68,8 @@ def test_q6_mmvq_matches_oracle(rows, cols, T, outl):
 
 
 @pytest.mark.parametrize("rows,cols", [(10240, 2560), (3000, 4096)])
-def test_q6_columns_bitwise_equal_single_token(rows, cols):
+@pytest.mark.parametrize("Q6", FMTS)
+def test_q6_columns_bitwise_equal_single_token(Q6, rows, cols):
     w = synth.make_weights(rows, cols, Q6, "q6inv")
     W = cu(w.buf)
     xq, xd, xs = strata.quantize_act(cu(synth.make_activations(8, cols, "q6inv")))
@@ -77,7 +81,8 @@ def test_q6_columns_bitwise_equal_single_token(rows, cols):
             assert np.array_equal(y[t].view(np.uint32), single[t][0].view(np.uint32)), (T, t)
 
 
-def test_q6_grouped_equals_separate_calls():
+@pytest.mark.parametrize("Q6", FMTS)
+def test_q6_grouped_equals_separate_calls(Q6):
     shapes, T = [(256, 512), (33, 768), (2048, 2048), (1, 256), (777, 1024)], 4
     probs, sep = [], []
     for k, (rows, cols) in enumerate(shapes):
@@ -94,8 +99,25 @@ def test_q6_grouped_equals_separate_calls():
         assert np.array_equal(y.cpu().numpy().view(np.uint32), s.view(np.uint32))
 
 
-def test_q6_rejects_partial_superblocks():
+def test_superblock_formats_reject_partial_superblocks():
     L = strata.lib()
     A16 = 0x10000
-    assert L.strata_mmvq_multi(A16, 64, 288, Q6, A16, A16, A16, 1, A16, None) == -2   # 288 % 256 != 0
-    assert L.strata_weight_bytes(10, 512, Q6) == 10 * 2 * 210
+    for fmt, per256 in ((synth.Q6, 210), (synth.Q4K, 148)):
+        assert L.strata_mmvq_multi(A16, 64, 288, fmt, A16, A16, A16, 1, A16, None) == -2   # 288 % 256 != 0
+        assert L.strata_weight_bytes(10, 512, fmt) == 10 * 2 * per256
+
+
+def test_q4k_head_argmax_matches_oracle():
+    """The vocabulary head in Q4K: ids exact (outside near ties), logits within the bound."""
+    vocab, cols, T = 20000, 2048, 4
+    w = synth.make_weights(vocab, cols, synth.Q4K, "q4khead")
+    xq, xd, xs = oracle.quantize_act(synth.make_activations(T, cols, "q4khead"))
+    lg = torch.empty((T, vocab), dtype=torch.float32, device="cuda")
+    ids = strata.head_argmax(cu(w.buf), vocab, cols, synth.Q4K, cu(xq), cu(xd), cu(xs), T, logits=lg).cpu().numpy()
+    ids_or, lg_or, A = oracle.head_argmax(w.buf, vocab, cols, synth.Q4K, xq, xd)
+    assert_within(lg.cpu().numpy(), lg_or, A, "q4k head")
+    for t in range(T):
+        assert ids[t] == int(np.argmax(lg.cpu().numpy()[t]))
+        top = np.sort(lg_or[t])[-2:]
+        if top[1] - top[0] > 2 * oracle.tolerance(A[t]).max():
+            assert ids[t] == ids_or[t]
