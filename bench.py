@@ -415,7 +415,8 @@ def main():
     if not args.no_moe:
         moe = bench_moe(torch, strata, synth, args)
         gemm = bench_prompt_gemm(torch, strata, synth)
-        q6 = bench_q6_layers(torch, strata, synth, hbm_peak)
+        q6 = {name: bench_superblock_layers(torch, strata, synth, hbm_peak, fmt)
+              for name, fmt in (("Q6", synth.Q6), ("Q4K", synth.Q4K))}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -438,7 +439,7 @@ def main():
             "per_T": per_T, "chained_launches": chained, "batch_head_margin": hb, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe, "prompt_gemm": gemm,
-            "q6_layers": q6,
+            "superblock_layers": q6,
             "device_error_word": strata.device_error(),
         }
         print(json.dumps(line), flush=True)
@@ -446,13 +447,15 @@ def main():
         dist.destroy_process_group()
 
 
-def bench_q6_layers(torch, strata, synth, hbm_peak, layers=16, reps=20):
-    """The window's layer projections in the Q6 super-block format (one grouped launch per window;
-    16 layers, 0.58 GB of weights, larger than L2) at T = 2 and 4: weight GB/s and HBM fraction."""
+def bench_superblock_layers(torch, strata, synth, hbm_peak, fmt, layers=16, reps=20):
+    """The window's layer projections in a 256-weight super-block format (Q6 or Q4K; one grouped
+    launch per window; 16 layers, 0.41-0.58 GB of weights, larger than L2) at T = 2 and 4: weight
+    GB/s and HBM fraction."""
     from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
-    wts = WindowWeights(layers=layers, device="cuda", key="q6-window", layer_fmt=synth.Q6)
+    name = {synth.Q6: "Q6", synth.Q4K: "Q4K"}[fmt]
+    wts = WindowWeights(layers=layers, device="cuda", key=f"{name}-window", layer_fmt=fmt)
     lay_bytes = sum(synth.weight_nbytes(r, c, f) for _, r, c, f in wts.shapes[:-1])
-    out = {"workload": f"{layers} layers x {{qkv 2048->5120, o 4096->2048, up 2048->6144, down 6144->2048}} Q6",
+    out = {"workload": f"{layers} layers x {{qkv 2048->5120, o 4096->2048, up 2048->6144, down 6144->2048}} {name}",
            "weight_bytes": lay_bytes}
     for T in (2, 4):
         win = VerifyWindow(wts, T)
