@@ -66,8 +66,15 @@ namespace strata {
 #define STRATA_MAXNREG 128
 #endif
 
-constexpr int kCW = STRATA_CW;            // consumer warps (+1 producer; at most 15: 16 warps x 128 registers fill the SM)
-constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+// Consumer warps (+1 producer; at most 15: 16 warps x 128 registers fill the SM), by T: 15 at
+// T = 2..4, where more warps hide more of the dp4a latency, else 12 (measured best on GB300). The
+// count only schedules work: each row's arithmetic does not depend on it.
+#ifndef STRATA_CW_MID
+#define STRATA_CW_MID 15
+#endif
+constexpr int cw_for(int T) { return (T >= 2 && T <= 4) ? STRATA_CW_MID : STRATA_CW; }
+constexpr int kCWMax = STRATA_CW > STRATA_CW_MID ? STRATA_CW : STRATA_CW_MID;
+static_assert(kCWMax <= 15, "at most 15 consumer warps");
 constexpr int kR = 4;                     // rows per row group (= per ring slot)
 constexpr int kMaxGroup = 192;            // matrices per grouped launch
 constexpr int kMaxGrid = 1024;
@@ -237,6 +244,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     constexpr int TPP = T <= 2 ? 2 : (T <= 4 ? 4 : 8);  // tokens padded for the scale vectors
     constexpr int NP = (T + 1) / 2;                      // token pairs
     constexpr int RX = XRec<T, FMT>::bytes;              // activation record per block
+    constexpr int kCW = cw_for(T);                       // consumer warps of this launch
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int s_abort;
 
@@ -834,7 +842,7 @@ int gemv_warps_per_row(int64_t cols, int fmt)
 
 // Chunks per ring stage: at most the group count (every group gets at most one row group of a
 // stage), about STRATA_STAGE_KB of codes and scales; a power of two when STRATA_SG_POW2 is set.
-static int stage_chunks(int64_t cols, int fmt, int ks)
+static int stage_chunks(int64_t cols, int fmt, int ks, int kCW)
 {
     const int64_t chunk = int64_t(kR) * ((cols / kQK) * (qbytes_of(fmt) + 2) + dbytes_per_row(cols, fmt));
     const int ng = kCW / ks;
@@ -874,8 +882,8 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
     pl.dstage = (fmt == 2 || fmt == 3) ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
-    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * kCW * 32) * 4 +
-                         size_t(kCW * 32) * 12;
+    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * cw_for(T) * 32) * 4 +
+                         size_t(cw_for(T) * 32) * 12;
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
     const size_t per = size_t(pl.cstage) + pl.sstage + pl.dstage;
     const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
@@ -893,7 +901,7 @@ bool gemv_shape_fits(int64_t cols, int fmt, int T)
     GemvMat m = {};
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks);
+    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T));
     const Plan pl = plan_for(T, &m, 1, fmt);
     return pl.ns >= 1 && pl.smem <= kSmemLimit;
 }
@@ -910,11 +918,11 @@ static cudaError_t launch_gemv(GemvParams<MAXM>& prm, const Plan& pl, int grid, 
     auto kern = gemv_kernel<FMT, T, MAXM, HEAD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), pl.smem, stream, prm);
+    return launch_pdl(kern, dim3(grid), dim3((cw_for(T) + 1) * 32), pl.smem, stream, prm);
 }
 
 static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq, const float* xd,
-                        const int32_t* xs, float* y, int chunk0)
+                        const int32_t* xs, float* y, int chunk0, int T)
 {
     GemvMat m;
     m.W = static_cast<const uint8_t*>(W);
@@ -925,7 +933,7 @@ static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, cons
     m.rows = int(rows);
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks);
+    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T));
     m.chunk0 = chunk0;
     return m;
 }
@@ -975,7 +983,7 @@ static cudaError_t single(const GemvMat& m, int fmt, int T, bool head, float* cv
 cudaError_t launch_mmvq(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq,
                         const float* xd, const int32_t* xs, int T, float* y, cudaStream_t stream)
 {
-    const GemvMat m = make_mat(W, rows, cols, fmt, xq, xd, xs, y, 0);
+    const GemvMat m = make_mat(W, rows, cols, fmt, xq, xd, xs, y, 0, T);
     return single(m, fmt, T, false, nullptr, nullptr, stream, nullptr);
 }
 
@@ -991,7 +999,7 @@ static cudaError_t grouped_t(const strata_gemv_desc* d, int n, cudaStream_t stre
     int chunks = 0;
     std::vector<double> cum(1, 0.0);
     for (int i = 0; i < n; ++i) {
-        prm.m[i] = make_mat(d[i].W, d[i].rows, d[i].cols, FMT, d[i].xq, d[i].xd, d[i].xs, d[i].y, chunks);
+        prm.m[i] = make_mat(d[i].W, d[i].rows, d[i].cols, FMT, d[i].xq, d[i].xd, d[i].xs, d[i].y, chunks, T);
         const int nc = int((d[i].rows + kR - 1) / kR);
         const double cb = double(kR) * ((d[i].cols / kQK) * (qbytes_of(FMT) + 2) + dbytes_per_row(d[i].cols, FMT));
         for (int c = 0; c < nc; ++c) cum.push_back(cum.back() + cb);
@@ -1063,7 +1071,7 @@ cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int f
                                const float* xd, const int32_t* xs, int T, int32_t* ids, float* margin,
                                float* logits, void* workspace, cudaStream_t stream)
 {
-    const GemvMat m = make_mat(W, vocab, cols, fmt, xq, xd, xs, logits, 0);
+    const GemvMat m = make_mat(W, vocab, cols, fmt, xq, xd, xs, logits, 0, T);
     const int grid = head_grid(vocab);
     if (grid > head_grid_bound(vocab)) return cudaErrorInvalidValue;
     float* cv = static_cast<float*>(workspace);
