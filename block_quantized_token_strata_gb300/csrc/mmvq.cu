@@ -18,12 +18,13 @@
 //   * T only sets the trip count of loops over independent columns. Nothing else depends on it.
 //
 // Data movement (GB300): a producer warp streams each CTA's contiguous rows with bulk (TMA) copies
-// into a ring of shared-memory slots, one row group of four rows per slot, completion tracked by
-// mbarriers; it starts before the kernel waits on its predecessor (programmatic dependent launch),
-// so weight bytes are in flight while the previous kernel finishes. Eight consumer warps read
-// codes and scales from the slots (consecutive lanes, consecutive 16-byte words) and the T
-// activation columns from a shared-memory copy made once per matrix, laid out as the 16-byte
-// halves each dp4a chain consumes. Every wait is bounded; a timeout sets the device error word.
+// into a ring of shared-memory stages (several row groups of four rows each, up to STRATA_STAGE_KB),
+// completion tracked by mbarriers; it starts before the kernel waits on its predecessor
+// (programmatic dependent launch), so weight bytes are in flight while the previous kernel
+// finishes. 12 or 15 consumer warps (by T) read codes and scales from the stages (consecutive
+// lanes, consecutive 16-byte words) and the T activation columns from a shared-memory copy made
+// once per matrix, laid out as the 16-byte halves each dp4a chain consumes. Every wait is bounded;
+// a timeout sets the device error word.
 #include <float.h>
 #include <limits.h>
 
@@ -39,13 +40,13 @@ namespace strata {
 // stage size cap, ring budget, L2 prefetch distance, and the warps-per-row rule (at most KS_MAX
 // warps per row; KS doubles while every lane keeps at least KS_MINB/32 blocks).
 #ifndef STRATA_STAGE_KB
-#define STRATA_STAGE_KB 36
+#define STRATA_STAGE_KB 60
 #endif
 #ifndef STRATA_RING_KB
-#define STRATA_RING_KB 176
+#define STRATA_RING_KB 200
 #endif
 #ifndef STRATA_PF_STAGES
-#define STRATA_PF_STAGES 4
+#define STRATA_PF_STAGES 2
 #endif
 #ifndef STRATA_KS_MAX
 #define STRATA_KS_MAX 4
@@ -57,10 +58,10 @@ namespace strata {
 #define STRATA_CW 12
 #endif
 #ifndef STRATA_SG_POW2
-#define STRATA_SG_POW2 1
+#define STRATA_SG_POW2 0
 #endif
 #ifndef STRATA_NST_POW2
-#define STRATA_NST_POW2 1
+#define STRATA_NST_POW2 0
 #endif
 #ifndef STRATA_MAXNREG
 #define STRATA_MAXNREG 128
@@ -212,7 +213,7 @@ struct SegIter {
     __device__ void next() { gs = ge; ++mi; if (gs < g1) settle(); }
 };
 
-// Walks a CTA's chunks as ring stages: runs of 2^lsg row groups of one matrix (about 32 KB).
+// Walks a CTA's chunks as ring stages: runs of m.sg row groups of one matrix (up to STRATA_STAGE_KB).
 template <int MAXM>
 struct StageIter {
     SegIter<MAXM> seg;
