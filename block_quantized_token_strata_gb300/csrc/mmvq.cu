@@ -73,9 +73,15 @@ namespace strata {
 #ifndef STRATA_CW_MID
 #define STRATA_CW_MID 15
 #endif
-constexpr int cw_for(int T) { return (T >= 2 && T <= 4) ? STRATA_CW_MID : STRATA_CW; }
+#ifndef STRATA_CW_HEAD
+#define STRATA_CW_HEAD 12
+#endif
+// the vocabulary head (a single Q8 matrix with the argmax epilogue) keeps its own count
+constexpr int cw_for(int T, bool head = false) {
+    return head ? STRATA_CW_HEAD : ((T >= 2 && T <= 4) ? STRATA_CW_MID : STRATA_CW);
+}
 constexpr int kCWMax = STRATA_CW > STRATA_CW_MID ? STRATA_CW : STRATA_CW_MID;
-static_assert(kCWMax <= 15, "at most 15 consumer warps");
+static_assert(kCWMax <= 15 && STRATA_CW_HEAD <= 15, "at most 15 consumer warps");
 constexpr int kR = 4;                     // rows per row group (= per ring slot)
 constexpr int kMaxGroup = 192;            // matrices per grouped launch
 constexpr int kMaxGrid = 1024;
@@ -245,7 +251,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     constexpr int TPP = T <= 2 ? 2 : (T <= 4 ? 4 : 8);  // tokens padded for the scale vectors
     constexpr int NP = (T + 1) / 2;                      // token pairs
     constexpr int RX = XRec<T, FMT>::bytes;              // activation record per block
-    constexpr int kCW = cw_for(T);                       // consumer warps of this launch
+    constexpr int kCW = cw_for(T, HEAD);                 // consumer warps of this launch
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int s_abort;
 
@@ -843,16 +849,22 @@ int gemv_warps_per_row(int64_t cols, int fmt)
 
 // Chunks per ring stage: at most the group count (every group gets at most one row group of a
 // stage), about STRATA_STAGE_KB of codes and scales; a power of two when STRATA_SG_POW2 is set.
-static int stage_chunks(int64_t cols, int fmt, int ks, int kCW)
+#ifndef STRATA_STAGE_KB_HEAD
+#define STRATA_STAGE_KB_HEAD 36
+#endif
+// stage size cap: the head (one long Q8 matrix) prefers smaller stages up to T = 4
+static int stage_kb(int T, bool head) { return (head && T <= 4) ? STRATA_STAGE_KB_HEAD : STRATA_STAGE_KB; }
+
+static int stage_chunks(int64_t cols, int fmt, int ks, int kCW, int stage_kb_cap)
 {
     const int64_t chunk = int64_t(kR) * ((cols / kQK) * (qbytes_of(fmt) + 2) + dbytes_per_row(cols, fmt));
     const int ng = kCW / ks;
     if (STRATA_SG_POW2) {
         int l = 0;
-        while ((2 << l) <= ng && chunk * (2 << l) <= (int64_t(STRATA_STAGE_KB) << 10)) ++l;
+        while ((2 << l) <= ng && chunk * (2 << l) <= (int64_t(stage_kb_cap) << 10)) ++l;
         return 1 << l;
     }
-    int sg = int(std::min<int64_t>(ng, (int64_t(STRATA_STAGE_KB) << 10) / chunk));
+    int sg = int(std::min<int64_t>(ng, (int64_t(stage_kb_cap) << 10) / chunk));
     return std::max(sg, 1);
 }
 
@@ -867,7 +879,7 @@ constexpr int kPrefetchStages = STRATA_PF_STAGES;
 
 // Shared-memory plan: activation copy + fixed scratch + a ring of stages (sizes: the largest over
 // the launch's matrices), as many stages as fit in kRingBudget and shared memory (at least one).
-static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
+static Plan plan_for(int T, const GemvMat* ms, int n, int fmt, bool head = false)
 {
     Plan pl;
     size_t cmax = 0, smax = 0, dmax = 0;
@@ -883,8 +895,9 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
     pl.dstage = (fmt == 2 || fmt == 3) ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
-    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * cw_for(T) * 32) * 4 +
-                         size_t(cw_for(T) * 32) * 12;
+    const int cw = cw_for(T, head);
+    const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * cw * 32) * 4 +
+                         size_t(cw * 32) * 12;
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
     const size_t per = size_t(pl.cstage) + pl.sstage + pl.dstage;
     const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
@@ -897,14 +910,20 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt)
     return pl;
 }
 
-bool gemv_shape_fits(int64_t cols, int fmt, int T)
+static bool shape_fits_as(int64_t cols, int fmt, int T, bool head)
 {
     GemvMat m = {};
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T));
-    const Plan pl = plan_for(T, &m, 1, fmt);
+    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T, head), stage_kb(T, head));
+    const Plan pl = plan_for(T, &m, 1, fmt, head);
     return pl.ns >= 1 && pl.smem <= kSmemLimit;
+}
+
+// the shape can be launched both as a GEMV and as a head
+bool gemv_shape_fits(int64_t cols, int fmt, int T)
+{
+    return shape_fits_as(cols, fmt, T, false) && shape_fits_as(cols, fmt, T, true);
 }
 
 template <int FMT, int T, int MAXM, bool HEAD>
@@ -919,7 +938,7 @@ static cudaError_t launch_gemv(GemvParams<MAXM>& prm, const Plan& pl, int grid, 
     auto kern = gemv_kernel<FMT, T, MAXM, HEAD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3((cw_for(T) + 1) * 32), pl.smem, stream, prm);
+    return launch_pdl(kern, dim3(grid), dim3((cw_for(T, HEAD) + 1) * 32), pl.smem, stream, prm);
 }
 
 static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq, const float* xd,
@@ -934,7 +953,7 @@ static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, cons
     m.rows = int(rows);
     m.nb = int(cols / kQK);
     m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T));
+    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T), stage_kb(T, false));
     m.chunk0 = chunk0;
     return m;
 }
@@ -945,14 +964,16 @@ static cudaError_t single_t(const GemvMat& m, float* cv, int* ci, cudaStream_t s
     GemvParams<1> prm = {};
     prm.n_mat = 1;
     prm.n_chunk = (m.rows + kR - 1) / kR;
-    prm.m[0] = m;
+    GemvMat mm = m;
+    if (HEAD) mm.sg = stage_chunks(int64_t(m.nb) * kQK, FMT, m.ks, cw_for(T, true), stage_kb(T, true));
+    prm.m[0] = mm;
     prm.cand_val = cv;
     prm.cand_idx = ci;
     const int grid = std::min(prm.n_chunk, kCtasPerSm * device_sm_count());
     prm.cand_sec = (HEAD && ci) ? reinterpret_cast<float*>(ci + size_t(grid) * T) : nullptr;  // [T][grid] after ids
     if (grid_out) *grid_out = grid;
     if (HEAD && cv == nullptr) return cudaSuccess;  // size query
-    const Plan pl = plan_for(T, &m, 1, FMT);
+    const Plan pl = plan_for(T, &mm, 1, FMT, HEAD);
     if (pl.ns < 1) return cudaErrorInvalidValue;
     return launch_gemv<FMT, T, 1, HEAD>(prm, pl, grid, stream);
 }
