@@ -124,9 +124,10 @@ int strata_quantize_act(const float* x, int64_t n_rows, int64_t cols,
  *   W  : weight matrix [rows][cols] in `fmt` (layout above), 16-byte aligned.
  *   xq, xd, xs : quantized activations of T rows of `cols` (xq 16-byte aligned).
  *   y  : fp32 [T][rows] (token-major, rows contiguous), 4-byte aligned.
- *   1 <= T <= 8, rows >= 1, cols % 32 == 0, 32 <= cols <= 65536, T*cols <= 131072, and the
- *   staged activations (T*cols*1.25 bytes) plus one four-row slot of W must fit in shared memory
- *   (for example Q8 with cols 16384 at T = 8 does not): otherwise STRATA_ERR_SHAPE.
+ *   1 <= T <= 8, rows >= 1, cols % 32 == 0 (cols % 256 == 0 for STRATA_Q6 and STRATA_Q4K),
+ *   32 <= cols <= 65536, T*cols <= 131072, and the staged activations (T*cols*1.25 bytes, a little
+ *   more for Q6) plus one four-row slot of W must fit in shared memory (for example Q8 with cols
+ *   16384 at T = 8 does not): otherwise STRATA_ERR_SHAPE.
  *   Column t is bitwise identical for every T (see the block arithmetic above).
  *   Errors: NULL, SHAPE, T, FMT, ALIGN, CUDA.
  */
