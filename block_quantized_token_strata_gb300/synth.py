@@ -13,6 +13,7 @@ Distributions (the workload recipe):
     per 16 weights), super-block scale d = fp16(|N(0,1)| * 0.001);
   * Q4K (256-weight super-blocks with minimums): codes q ~ U{0..15}, per 32 weights a scale
     sc ~ U{0..63} and a minimum m ~ U{0..63}, per 256 weights d and dmin = fp16(|N(0,1)| * 0.001);
+  * Q5K: as Q4K with codes q ~ U{0..31};
   * activations x ~ N(0,1) fp32, optionally with a Bernoulli(0.01) mask of elements scaled x20;
   * MoE routing: k distinct experts per token drawn without replacement from a Zipf(1.1)
     law over expert ranks, p_e proportional to (e+1)^-1.1, draw order = slot order.
@@ -25,8 +26,8 @@ import numpy as np
 
 QK = 32
 QKS = 256  # Q6 super-block
-Q4, Q8, Q6, Q4K = 0, 1, 2, 3
-_QBYTES = {Q4: 16, Q8: 32, Q6: 24, Q4K: 16}
+Q4, Q8, Q6, Q4K, Q5K = 0, 1, 2, 3, 4
+_QBYTES = {Q4: 16, Q8: 32, Q6: 24, Q4K: 16, Q5K: 20}
 
 
 def _rng(*key) -> np.random.Generator:
@@ -42,8 +43,8 @@ def _rng(*key) -> np.random.Generator:
 
 def weight_nbytes(rows: int, cols: int, fmt: int) -> int:
     nb = rows * (cols // QK)
-    # per super-block: Q6 one fp16 d, Q4K fp16 d and dmin
-    extra = rows * (cols // QKS) * (2 if fmt == Q6 else 4) if fmt in (Q6, Q4K) else 0
+    # per super-block: Q6 one fp16 d, Q4K / Q5K fp16 d and dmin
+    extra = rows * (cols // QKS) * (2 if fmt == Q6 else 4) if fmt in (Q6, Q4K, Q5K) else 0
     return nb * (_QBYTES[fmt] + 2) + extra
 
 
@@ -104,6 +105,25 @@ def make_q4k_buffer(q: np.ndarray, sc: np.ndarray, mn: np.ndarray, d: np.ndarray
     return np.concatenate([code.reshape(-1), smp.reshape(-1), dd.reshape(-1).view(np.uint8)])
 
 
+def make_q5k_buffer(q: np.ndarray, sc: np.ndarray, mn: np.ndarray, d: np.ndarray, dmin: np.ndarray) -> np.ndarray:
+    """Lay out Q5K codes q uint8 [rows][cols] (0..31), per-32 scales and minimums and per-256 fp16
+    d, dmin in the planar Q5K format: per row its Q4-style nibble blocks, then one 32-bit word per
+    block with the fifth bit of the k-th code of four-code group g (groups of elements 0-15, then
+    16-31) at bit 8k + g; then the (sc, m) plane and the (d, dmin) plane as in Q4K."""
+    rows, cols = q.shape
+    nb = cols // QK
+    qb = q.reshape(rows, nb, 32).astype(np.uint32)
+    nib = ((qb[:, :, :16] & 15) | ((qb[:, :, 16:] & 15) << 4)).astype(np.uint8)
+    fifth = (qb >> 4) & 1                                   # [rows][nb][32]
+    groups = fifth.reshape(rows, nb, 8, 4)                  # group g = elements 4g..4g+3
+    shifts = (8 * np.arange(4)[None, None, None, :] + np.arange(8)[None, None, :, None]).astype(np.uint32)
+    words = (groups << shifts).sum(axis=(2, 3)).astype(np.uint32)  # distinct bits: the sum is an OR
+    code = np.concatenate([nib.reshape(rows, nb * 16), words.view(np.uint8).reshape(rows, nb * 4)], axis=1)
+    smp = np.stack([np.asarray(sc, np.uint8), np.asarray(mn, np.uint8)], axis=-1)
+    dd = np.stack([np.asarray(d, np.float16), np.asarray(dmin, np.float16)], axis=-1)
+    return np.concatenate([code.reshape(-1), smp.reshape(-1), dd.reshape(-1).view(np.uint8)])
+
+
 def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
     """A seeded [rows][cols] matrix in Q4, Q8 or Q6 (planar layout, see include/strata.h)."""
     if cols % QK or rows <= 0:
@@ -125,6 +145,15 @@ def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
         d = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
         dmin = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
         return Weights(rows, cols, fmt, make_q4k_buffer(q, sc, mn, d, dmin))
+    if fmt == Q5K:
+        if cols % QKS:
+            raise ValueError("Q5K needs cols % 256 == 0")
+        q = rng.integers(0, 32, size=(rows, cols), dtype=np.uint8)
+        sc = rng.integers(0, 64, size=(rows, cols // QK), dtype=np.uint8)
+        mn = rng.integers(0, 64, size=(rows, cols // QK), dtype=np.uint8)
+        d = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
+        dmin = (np.abs(rng.standard_normal((rows, cols // QKS))) * 0.001).astype(np.float16)
+        return Weights(rows, cols, fmt, make_q5k_buffer(q, sc, mn, d, dmin))
     nb = rows * (cols // QK)
     d = (np.abs(rng.standard_normal(nb)) * 0.01).astype(np.float16)
     if fmt == Q4:

@@ -22,6 +22,10 @@
  *   dots per 16 weights (one term per sub-scale); Q4K (the pages' 4-bit super-block type with
  *   minimums): per 32 weights a 6-bit scale sc and minimum m, per 256 weights fp16 d and dmin, 4-bit
  *   codes q, w = d*sc*q - dmin*m, two terms per 32 weights (d*sc*d_x*isum and -dmin*m*d_x*sum x);
+ *   Q5K (the pages' 5-bit super-block type, whose dots take the same two exact forms as Q4K's):
+ *   Q4K with 5-bit codes q in 0..31; a row's code plane holds its Q4-style nibble blocks, then one
+ *   32-bit little-endian word per block whose bit 8k + w is the fifth bit of the k-th code of
+ *   four-code group w (groups 0..3 = elements 0..15 in fours, 4..7 = elements 16..31);
  *   activations: per 32 values amax, d = amax/127 (fp32), q = roundf(x/d) via x*(1/d),
  *   s = sum q; MoE hidden h = silu(g)*u with silu(g) = g/(1+exp(-g)), re-quantized the same way.
  *
@@ -41,6 +45,7 @@
 #define OR_Q8 1
 #define OR_Q6 2
 #define OR_Q4K 3
+#define OR_Q5K 4
 
 /* ---- IEEE 754 binary16 -> double, from the format's definition ---------------------------- */
 double or_half_to_double(uint16_t h)
@@ -60,7 +65,12 @@ double or_half_to_double(uint16_t h)
 }
 
 /* ---- the planar weight layout ---------------------------------------------------------------- */
-static int64_t qbytes(int fmt) { return (fmt == OR_Q4 || fmt == OR_Q4K) ? 16 : (fmt == OR_Q8 ? 32 : 24); }
+static int64_t qbytes(int fmt)
+{
+    if (fmt == OR_Q4 || fmt == OR_Q4K) return 16;
+    if (fmt == OR_Q5K) return 20;  /* per block in the code plane: 16 nibble bytes + a 4-byte word */
+    return fmt == OR_Q8 ? 32 : 24;
+}
 
 /* Q4/Q8: the fp16 scale of block (r, b). Q6: the fp16 d of the super-block holding block b, which
  * sits after the code plane (24 bytes a block) and the sub-scale plane (2 int8 a block). */
@@ -69,23 +79,24 @@ static double block_scale(const uint8_t* W, int64_t rows, int64_t nb, int fmt, i
     const uint8_t* p;
     if (fmt == OR_Q6)
         p = W + rows * nb * 26 + 2 * (r * (nb / 8) + b / 8);
-    else if (fmt == OR_Q4K)  /* d of the super-block (dmin follows it) */
-        p = W + rows * nb * 18 + 4 * (r * (nb / 8) + b / 8);
+    else if (fmt == OR_Q4K || fmt == OR_Q5K)  /* d of the super-block (dmin follows it) */
+        p = W + rows * nb * (qbytes(fmt) + 2) + 4 * (r * (nb / 8) + b / 8);
     else
         p = W + rows * nb * qbytes(fmt) + 2 * (r * nb + b);
     uint16_t bits = (uint16_t)(p[0] | (p[1] << 8));
     return or_half_to_double(bits);
 }
 
-/* Q4K: the super-block's fp16 dmin, and block (r, b)'s 6-bit scale (k = 0) or minimum (k = 1) */
-static double q4k_dmin(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, int64_t b)
+/* Q4K / Q5K: the super-block's fp16 dmin, and block (r, b)'s 6-bit scale (k = 0) or minimum (k = 1);
+ * both planes follow the code plane */
+static double kq_dmin(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t r, int64_t b)
 {
-    const uint8_t* p = W + rows * nb * 18 + 4 * (r * (nb / 8) + b / 8) + 2;
+    const uint8_t* p = W + rows * nb * (qbytes(fmt) + 2) + 4 * (r * (nb / 8) + b / 8) + 2;
     return or_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
 }
-static int q4k_scale_min(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, int64_t b, int k)
+static int kq_scale_min(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t r, int64_t b, int k)
 {
-    return (int)W[rows * nb * 16 + 2 * (r * nb + b) + k];
+    return (int)W[rows * nb * qbytes(fmt) + 2 * (r * nb + b) + k];
 }
 
 /* Q6: the int8 sub-scale of half h (elements 16h..16h+15) of block (r, b) */
@@ -97,6 +108,18 @@ static int q6_subscale(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, in
 /* weight code of element j (0..31) of block (r, b), already offset: Q4 q-8, Q8 q */
 static int weight_code(const uint8_t* W, int64_t nb, int fmt, int64_t r, int64_t b, int j)
 {
+    if (fmt == OR_Q5K) {
+        /* the row's nibble blocks, then its fifth-bit words; code = low nibble | fifth bit << 4 */
+        const uint8_t* row = W + r * nb * 20;
+        int byte = row[16 * b + (j & 15)];
+        int low = (j < 16) ? (byte & 0x0F) : (byte >> 4);
+        const uint8_t* hw = row + 16 * nb + 4 * b;
+        uint32_t bits = (uint32_t)hw[0] | ((uint32_t)hw[1] << 8) | ((uint32_t)hw[2] << 16) | ((uint32_t)hw[3] << 24);
+        int group = (j < 16) ? j / 4 : 4 + (j - 16) / 4;
+        int k = j % 4;
+        int fifth = (int)((bits >> (8 * k + group)) & 1u);
+        return low | (fifth << 4);
+    }
     const uint8_t* blk = W + (r * nb + b) * qbytes(fmt);
     if (fmt == OR_Q4 || fmt == OR_Q4K) {  /* Q4K codes carry no offset: its minimum does that */
         int byte = blk[j & 15];
@@ -179,12 +202,12 @@ static void row_dot(const uint8_t* W, int64_t rows, int64_t nb, int fmt, int64_t
 {
     double acc = 0.0, aabs = 0.0;
     for (int64_t b = 0; b < nb; ++b) {
-        if (fmt == OR_Q4K) {  /* d*sc*d_x*isum, then -dmin*m*d_x*(sum of the block's x codes) */
+        if (fmt == OR_Q4K || fmt == OR_Q5K) {  /* d*sc*d_x*isum, then -dmin*m*d_x*(sum of the block's x codes) */
             int64_t isum = block_isum(W, rows, nb, fmt, r, b, xq_row + 32 * b), xsum = 0;
             for (int j = 0; j < 32; ++j) xsum += xq_row[32 * b + j];
-            double t1 = block_scale(W, rows, nb, fmt, r, b) * (double)q4k_scale_min(W, rows, nb, r, b, 0) *
+            double t1 = block_scale(W, rows, nb, fmt, r, b) * (double)kq_scale_min(W, rows, nb, fmt, r, b, 0) *
                         (double)xd_row[b] * (double)isum;
-            double t2 = -q4k_dmin(W, rows, nb, r, b) * (double)q4k_scale_min(W, rows, nb, r, b, 1) *
+            double t2 = -kq_dmin(W, rows, nb, fmt, r, b) * (double)kq_scale_min(W, rows, nb, fmt, r, b, 1) *
                         (double)xd_row[b] * (double)xsum;
             acc += t1;
             acc += t2;

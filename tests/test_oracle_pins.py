@@ -416,3 +416,82 @@ def test_q4k_brute_force_dense(orc):
     assert np.array_equal(isum.reshape(T, rows, cols // 32), want)
     from block_quantized_token_strata_gb300 import synth
     assert np.array_equal(synth.make_q4k_buffer(q, sc, mn, d, dmin), W)
+
+
+# ---- Q5K (5-bit codes, 6-bit scale and minimum per 32 weights, fp16 d and dmin per 256) --------------
+def pack_q5k(q, sc, mn, d, dmin) -> np.ndarray:
+    """This test's own packer: per row, the Q4-style nibble bytes of every block, then per block a
+    little-endian 32-bit word whose bit 8k + g is the fifth bit of element 4g + k (g < 4) or
+    16 + 4(g - 4) + k (g >= 4); then (sc, m) byte pairs per block and (d, dmin) fp16 pairs per 256."""
+    rows, cols = q.shape
+    out = bytearray()
+    for r in range(rows):
+        nib, words = bytearray(), bytearray()
+        for b in range(cols // 32):
+            blk = [int(v) for v in q[r, 32 * b:32 * b + 32]]
+            nib += bytes((blk[j] & 15) | ((blk[j + 16] & 15) << 4) for j in range(16))
+            word = 0
+            for j in range(32):
+                g = j // 4 if j < 16 else 4 + (j - 16) // 4
+                word |= ((blk[j] >> 4) & 1) << (8 * (j % 4) + g)
+            words += word.to_bytes(4, "little")
+        out += nib + words
+    for r in range(rows):
+        for b in range(cols // 32):
+            out += bytes([int(sc[r, b]), int(mn[r, b])])
+    for r in range(rows):
+        for k in range(cols // 256):
+            out += np.array([d[r, k], dmin[r, k]], np.float16).tobytes()
+    return np.frombuffer(bytes(out), np.uint8).copy()
+
+
+def test_q5k_one_superblock_by_hand(orc):
+    """cols = 256, x codes all 1 with d_x = 1, d = dmin = 1. Code 31 with sc 1 and m 0 gives
+    8 blocks x 32 x 31 = 7936; code 16 (only the fifth bit set) with sc 2, m 3 gives
+    8 x 32 x (2*16 - 3) = 7424; code 17 with sc 0 and m 1 gives -256; a code whose fifth bit is clear
+    (15) matches Q4K's 3840."""
+    xq = np.ones((1, 256), np.int8)
+    xd = np.ones((1, 8), np.float32)
+    one = np.ones((1, 1), np.float16)
+    for code, sc, mn, want in [(31, 1, 0, 7936.0), (16, 2, 3, 7424.0), (17, 0, 1, -256.0), (15, 1, 0, 3840.0)]:
+        W = pack_q5k(np.full((1, 256), code, np.uint8), np.full((1, 8), sc), np.full((1, 8), mn), one, one)
+        y, A = orc.mmvq(W, 1, 256, 4, xq, xd)
+        assert y[0, 0] == want, (code, sc, mn, y)
+
+
+def test_q5k_fifth_bit_positions(orc):
+    """One code 16 at element j, all others 0, x = one-hot at element j: the block dot is 16 exactly
+    for the one matching element, 0 for every other placement (a wrong bit index shows here)."""
+    for j in range(32):
+        q = np.zeros((1, 256), np.uint8)
+        q[0, j] = 16
+        W = pack_q5k(q, np.ones((1, 8), np.uint8), np.zeros((1, 8), np.uint8),
+                     np.ones((1, 1), np.float16), np.ones((1, 1), np.float16))
+        for i in (j, (j + 1) % 32, (j + 4) % 32, (j + 16) % 32):
+            xq = np.zeros((1, 256), np.int8)
+            xq[0, i] = 1
+            isum = orc.block_dots(W, 1, 256, 4, xq)
+            assert isum[0, 0, 0] == (16 if i == j else 0), (j, i, isum[0, 0, 0])
+
+
+def test_q5k_brute_force_dense(orc):
+    rng = np.random.default_rng(29)
+    rows, cols, T = 5, 768, 3
+    q = rng.integers(0, 32, size=(rows, cols)).astype(np.uint8)
+    sc = rng.integers(0, 64, size=(rows, cols // 32)).astype(np.uint8)
+    mn = rng.integers(0, 64, size=(rows, cols // 32)).astype(np.uint8)
+    d = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+    dmin = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+    W = pack_q5k(q, sc, mn, d, dmin)
+    assert W.size == rows * (cols // 256) * 180
+    xq, xd, _ = orc.quantize_act(rng.standard_normal((T, cols)).astype(np.float32))
+    w = (d.astype(np.float64).repeat(256, axis=1) * sc.astype(np.float64).repeat(32, axis=1) * q
+         - dmin.astype(np.float64).repeat(256, axis=1) * mn.astype(np.float64).repeat(32, axis=1))
+    ref = (xq.astype(np.float64) * xd.astype(np.float64).repeat(32, axis=1)) @ w.T
+    y, A = orc.mmvq(W, rows, cols, 4, xq, xd)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    isum = orc.block_dots(W, rows, cols, 4, xq)
+    want = np.einsum("rbj,tbj->trb", q.astype(np.int64).reshape(rows, -1, 32), xq.astype(np.int64).reshape(T, -1, 32))
+    assert np.array_equal(isum.reshape(T, rows, cols // 32), want)
+    from block_quantized_token_strata_gb300 import synth
+    assert np.array_equal(synth.make_q5k_buffer(q, sc, mn, d, dmin), W)
