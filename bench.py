@@ -416,7 +416,7 @@ def main():
         moe = bench_moe(torch, strata, synth, args)
         gemm = bench_prompt_gemm(torch, strata, synth)
         q6 = {name: bench_superblock_layers(torch, strata, synth, hbm_peak, fmt)
-              for name, fmt in (("Q6", synth.Q6), ("Q4K", synth.Q4K))}
+              for name, fmt in (("Q6", synth.Q6), ("Q4K", synth.Q4K), ("Q5K", synth.Q5K))}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -448,11 +448,11 @@ def main():
 
 
 def bench_superblock_layers(torch, strata, synth, hbm_peak, fmt, layers=16, reps=20):
-    """The window's layer projections in a 256-weight super-block format (Q6 or Q4K; one grouped
+    """The window's layer projections in a 256-weight super-block format (Q6, Q4K or Q5K; one grouped
     launch per window; 16 layers, 0.41-0.58 GB of weights, larger than L2) at T = 2 and 4: weight
     GB/s and HBM fraction."""
     from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
-    name = {synth.Q6: "Q6", synth.Q4K: "Q4K"}[fmt]
+    name = {synth.Q6: "Q6", synth.Q4K: "Q4K", synth.Q5K: "Q5K"}[fmt]
     wts = WindowWeights(layers=layers, device="cuda", key=f"{name}-window", layer_fmt=fmt)
     lay_bytes = sum(synth.weight_nbytes(r, c, f) for _, r, c, f in wts.shapes[:-1])
     out = {"workload": f"{layers} layers x {{qkv 2048->5120, o 4096->2048, up 2048->6144, down 6144->2048}} {name}",

@@ -16,9 +16,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? STRATA_OK : STRATA_ER
 
 int check_matrix(int64_t rows, int64_t cols, int fmt)
 {
-    if (fmt != STRATA_Q4 && fmt != STRATA_Q8 && fmt != STRATA_Q6 && fmt != STRATA_Q4K) return STRATA_ERR_FMT;
+    if (fmt != STRATA_Q4 && fmt != STRATA_Q8 && fmt != STRATA_Q6 && fmt != STRATA_Q4K && fmt != STRATA_Q5K)
+        return STRATA_ERR_FMT;
     if (rows <= 0 || cols < 32 || cols % 32 != 0) return STRATA_ERR_SHAPE;
-    if ((fmt == STRATA_Q6 || fmt == STRATA_Q4K) && cols % 256 != 0) return STRATA_ERR_SHAPE;
+    if ((fmt == STRATA_Q6 || fmt == STRATA_Q4K || fmt == STRATA_Q5K) && cols % 256 != 0) return STRATA_ERR_SHAPE;
     if (rows > INT_MAX / 2 || cols > 65536) return STRATA_ERR_SHAPE;
     return STRATA_OK;
 }
@@ -55,6 +56,7 @@ size_t strata_weight_bytes(int64_t rows, int64_t cols, int fmt)
     if (check_matrix(rows, cols, fmt) != STRATA_OK) return 0;
     if (fmt == STRATA_Q6) return size_t(rows) * size_t(cols / 256) * 210u;
     if (fmt == STRATA_Q4K) return size_t(rows) * size_t(cols / 256) * 148u;
+    if (fmt == STRATA_Q5K) return size_t(rows) * size_t(cols / 256) * 180u;
     return size_t(rows) * size_t(cols / 32) * (fmt == STRATA_Q4 ? 18u : 34u);
 }
 
@@ -86,7 +88,8 @@ int strata_mmvq_grouped(const strata_gemv_desc* descs, int n, int fmt, int T, cu
 {
     if (!descs) return STRATA_ERR_NULL;
     if (n < 1 || n > kMaxGroupedMatrices) return STRATA_ERR_SHAPE;
-    if (fmt != STRATA_Q4 && fmt != STRATA_Q8 && fmt != STRATA_Q6 && fmt != STRATA_Q4K) return STRATA_ERR_FMT;
+    if (fmt != STRATA_Q4 && fmt != STRATA_Q8 && fmt != STRATA_Q6 && fmt != STRATA_Q4K && fmt != STRATA_Q5K)
+        return STRATA_ERR_FMT;
     if (T < 1 || T > STRATA_MAX_T) return STRATA_ERR_T;
     int64_t cols_max = 0, total_rows = 0;
     for (int i = 0; i < n; ++i) {

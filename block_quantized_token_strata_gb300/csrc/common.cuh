@@ -147,6 +147,21 @@ __device__ __forceinline__ int dot_q8(const uint4 w0, const uint4 w1, const uint
     c = __dp4a(int(w1.w), int(xhi.w), c);
     return c;
 }
+// Q5K block (codes 0..31, no offset) against one token's 32 activation codes, onto c. w = the Q4-style
+// nibble bytes (byte j: low 4 bits of code j, of code j+16 in the high nibble); hb = the fifth bits,
+// code k of four-code group g (g = 0..3: codes 4g..4g+3; g = 4..7: codes 16+4(g-4)..) at bit 8k + g,
+// so one shift and one mask put a group's four fifth bits at bit 4 of its four bytes.
+__device__ __forceinline__ int dot_q5(const uint4 w, uint32_t hb, const uint4 xlo, const uint4 xhi, int c) {
+    c = __dp4a(int((w.x & 0x0F0F0F0Fu) | ((hb << 4) & 0x10101010u)), int(xlo.x), c);
+    c = __dp4a(int((w.y & 0x0F0F0F0Fu) | ((hb << 3) & 0x10101010u)), int(xlo.y), c);
+    c = __dp4a(int((w.z & 0x0F0F0F0Fu) | ((hb << 2) & 0x10101010u)), int(xlo.z), c);
+    c = __dp4a(int((w.w & 0x0F0F0F0Fu) | ((hb << 1) & 0x10101010u)), int(xlo.w), c);
+    c = __dp4a(int(((w.x >> 4) & 0x0F0F0F0Fu) | (hb & 0x10101010u)), int(xhi.x), c);
+    c = __dp4a(int(((w.y >> 4) & 0x0F0F0F0Fu) | ((hb >> 1) & 0x10101010u)), int(xhi.y), c);
+    c = __dp4a(int(((w.z >> 4) & 0x0F0F0F0Fu) | ((hb >> 2) & 0x10101010u)), int(xhi.z), c);
+    c = __dp4a(int(((w.w >> 4) & 0x0F0F0F0Fu) | ((hb >> 3) & 0x10101010u)), int(xhi.w), c);
+    return c;
+}
 // Q6 block codes as dp4a operands: words 0..3 hold elements 0..15, words 4..7 elements 16..31, one
 // 6-bit code q (0..63) per byte. Layout: lo0/lo1 = code bytes 0..15 (byte j: low 4 bits of element j
 // in bits 0-3, of element j+16 in bits 4-7), hi = bytes 16..23 (byte 16+i: the high 2 bits of

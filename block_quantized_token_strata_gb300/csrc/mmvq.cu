@@ -100,8 +100,11 @@ template <> struct FmtInfo<2> { static constexpr int kQB = 24; };
 // Q4K: Q4's 16 code bytes (codes 0..15, no offset); its "scale plane" holds each block's 6-bit scale
 // and minimum, the third plane fp16 d and dmin per 8 blocks
 template <> struct FmtInfo<3> { static constexpr int kQB = 16; };
+// Q5K: Q4K with 5-bit codes; a row's code plane is its nibble blocks (16 bytes each) followed by one
+// 32-bit word of fifth bits per block, so kQB counts 20 bytes a block
+template <> struct FmtInfo<4> { static constexpr int kQB = 20; };
 // bytes per super-block (256 weights) in the third plane
-template <int FMT> struct SuperInfo { static constexpr int kDB = FMT == 2 ? 2 : (FMT == 3 ? 4 : 0); };
+template <int FMT> struct SuperInfo { static constexpr int kDB = FMT == 2 ? 2 : ((FMT == 3 || FMT == 4) ? 4 : 0); };
 
 struct GemvMat {
     const uint8_t* W;
@@ -418,11 +421,11 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
             for (int i = threadIdx.x; i < nb * TPP; i += kCW * 32) {
                 const int b = i / TPP, t = i - (i / TPP) * TPP;
                 float d = 0.0f;
-                int c0 = (FMT == 3) ? 0 : kMagicBits, c1 = kMagicBits;  // Q4K: the block sum as a float
+                int c0 = (FMT == 3 || FMT == 4) ? 0 : kMagicBits, c1 = kMagicBits;  // Q4K/Q5K: the block sum as a float
                 if (t < T) {
                     d = __ldg(m.xd + t * nb + b);
                     if (FMT == 0) c0 = kMagicBits - 8 * __ldg(m.xs + t * nb + b);
-                    if (FMT == 3) c0 = __float_as_int(float(__ldg(m.xs + t * nb + b)));  // exact: |s| <= 4064
+                    if (FMT == 3 || FMT == 4) c0 = __float_as_int(float(__ldg(m.xs + t * nb + b)));  // exact: |s| <= 4064
                     if (FMT == 2) {
                         // Q6 codes stand for q - 32 and carry one sub-scale per 16: seed each half's chain
                         // with -32 times that half's activation sum
@@ -549,23 +552,27 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                                 }
                             }
                         }
-                    } else if constexpr (FMT == 3) {
+                    } else if constexpr (FMT == 3 || FMT == 4) {
                         // Q4K: per block 16 code bytes (codes 0..15), a 6-bit scale and minimum; per 8
-                        // blocks fp16 d and dmin. Terms: (d*sc*d_x)*isum, then (-dmin*m*d_x)*sum(x)
+                        // blocks fp16 d and dmin. Terms: (d*sc*d_x)*isum, then (-dmin*m*d_x)*sum(x).
+                        // Q5K: the same with each block's fifth-bit word after the row's nibble blocks
                         const uintptr_t dsrc = reinterpret_cast<uintptr_t>(m.W + size_t(rows) * nb * (QB + 2) +
                                                                            size_t(r0s) * (nb / 8) * 4);
                         const unsigned short* dpl = reinterpret_cast<const unsigned short*>(
                             dring + s * p.dstage + int(dsrc & 15) + pos * (kR * 4) * (nb / 8));
                         const int ns = nb / 8;
                         for (int kb = gl; kb < nb; kb += G) {
-                            const uint8_t* wp = cb + kb * QB;
+                            const uint8_t* wp = cb + kb * 16;
+                            const uint8_t* hp = cb + 16 * nb + kb * 4;  // Q5K: the block's fifth-bit word
                             const unsigned short* sp = sc + kb;
                             const uint8_t* xr = xsm + kb * RX;
                             uint4 w[kR];
+                            uint32_t hbw[kR];
                             f32x2 sc2[kR], mn2[kR];
 #pragma unroll
                             for (int r = 0; r < kR; ++r) {
                                 w[r] = *reinterpret_cast<const uint4*>(wp + r * rsw);
+                                hbw[r] = (FMT == 4) ? *reinterpret_cast<const uint32_t*>(hp + r * rsw) : 0u;
                                 const unsigned short su = sp[r * nb];
                                 const int di = 2 * (r * ns + (kb >> 3));
                                 const float dd = __half2float(__ushort_as_half(dpl[di]));
@@ -598,8 +605,14 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                                 const f32x2 xs2 = pack_f2(xsv[ta], xsv[tb]);
 #pragma unroll
                                 for (int r = 0; r < kR; ++r) {
-                                    const int ca = dot_q4(w[r], xla, xha, kMagicBits);
-                                    const int cbv = (tb < T) ? dot_q4(w[r], xlb, xhb, kMagicBits) : kMagicBits;
+                                    int ca, cbv;
+                                    if constexpr (FMT == 4) {
+                                        ca = dot_q5(w[r], hbw[r], xla, xha, kMagicBits);
+                                        cbv = (tb < T) ? dot_q5(w[r], hbw[r], xlb, xhb, kMagicBits) : kMagicBits;
+                                    } else {
+                                        ca = dot_q4(w[r], xla, xha, kMagicBits);
+                                        cbv = (tb < T) ? dot_q4(w[r], xlb, xhb, kMagicBits) : kMagicBits;
+                                    }
                                     const f32x2 f2 = add_f2(pack_f2(__int_as_float(ca), __int_as_float(cbv)), negm);
                                     acc[r][q] = fma_f2(mul_f2(sc2[r], dx2), f2, acc[r][q]);
                                     acc[r][q] = fma_f2(mul_f2(mn2[r], dx2), xs2, acc[r][q]);
@@ -805,6 +818,17 @@ __global__ void __launch_bounds__(256) block_dots_kernel(const uint8_t* __restri
         }
         return;
     }
+    if constexpr (FMT == 4) {
+        // Q5K: codes 0..31, the row's nibble blocks then its fifth-bit words; no offset
+        const uint8_t* row = W + size_t(r) * nb * 20;
+        const uint4 w = ld_stream_v4(row + size_t(b) * 16);
+        const uint32_t hb = *reinterpret_cast<const uint32_t*>(row + size_t(nb) * 16 + size_t(b) * 4);
+        for (int t = 0; t < T; ++t) {
+            const uint4* xp = reinterpret_cast<const uint4*>(xq + size_t(t) * nb * 32 + size_t(b) * 32);
+            isum[(size_t(t) * rows + r) * nb + b] = dot_q5(w, hb, xp[0], xp[1], kMagicBits) - kMagicBits;
+        }
+        return;
+    }
     const uint4 w0 = ld_stream_v4(W + size_t(i) * QB);
     const uint4 w1 = (QB == 32) ? ld_stream_v4(W + size_t(i) * QB + 16) : w0;
     for (int t = 0; t < T; ++t) {
@@ -831,9 +855,9 @@ int device_sm_count()
     return cache[dev];
 }
 
-static int qbytes_of(int fmt) { return (fmt == 0 || fmt == 3) ? 16 : (fmt == 1 ? 32 : 24); }
+static int qbytes_of(int fmt) { return (fmt == 0 || fmt == 3) ? 16 : (fmt == 1 ? 32 : (fmt == 4 ? 20 : 24)); }
 // weight bytes per row group beyond the codes and the per-block 2-byte plane: Q6's super-block d
-static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : (fmt == 3 ? (cols / 256) * 4 : 0); }
+static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : ((fmt == 3 || fmt == 4) ? (cols / 256) * 4 : 0); }
 
 // Warps per row: a function of (cols, fmt) only, so every launch of a shape (any T, single or
 // grouped) sums each row in the same order. As few warps as keep at least two blocks per lane
@@ -894,7 +918,7 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt, bool head = false
     pl.nb_max = nb_max;
     pl.cstage = int((cmax + 127) & ~size_t(127));
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
-    pl.dstage = (fmt == 2 || fmt == 3) ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
+    pl.dstage = (fmt == 2 || fmt == 3 || fmt == 4) ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
     const int cw = cw_for(T, head);
     const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * cw * 32) * 4 +
                          size_t(cw * 32) * 12;
@@ -999,6 +1023,7 @@ static cudaError_t single(const GemvMat& m, int fmt, int T, bool head, float* cv
     if (fmt == 0) return head ? single_f<0, true>(m, T, cv, ci, s, g) : single_f<0, false>(m, T, cv, ci, s, g);
     if (fmt == 2) return head ? single_f<2, true>(m, T, cv, ci, s, g) : single_f<2, false>(m, T, cv, ci, s, g);
     if (fmt == 3) return head ? single_f<3, true>(m, T, cv, ci, s, g) : single_f<3, false>(m, T, cv, ci, s, g);
+    if (fmt == 4) return head ? single_f<4, true>(m, T, cv, ci, s, g) : single_f<4, false>(m, T, cv, ci, s, g);
     return head ? single_f<1, true>(m, T, cv, ci, s, g) : single_f<1, false>(m, T, cv, ci, s, g);
 }
 
@@ -1061,6 +1086,7 @@ cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T
 {
     if (fmt == 2) return grouped_f<2>(d, n, T, stream);
     if (fmt == 3) return grouped_f<3>(d, n, T, stream);
+    if (fmt == 4) return grouped_f<4>(d, n, T, stream);
     return fmt == 0 ? grouped_f<0>(d, n, T, stream) : grouped_f<1>(d, n, T, stream);
 }
 
@@ -1119,6 +1145,8 @@ cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt
         return launch_pdl(block_dots_kernel<3>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
     if (fmt == 2)
         return launch_pdl(block_dots_kernel<2>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
+    if (fmt == 4)
+        return launch_pdl(block_dots_kernel<4>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
     return launch_pdl(block_dots_kernel<1>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
 }
 

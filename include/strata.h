@@ -54,8 +54,15 @@
  *                then rows*(cols/256) pairs of fp16 (d, dmin) per super-block. The weight is
  *                w = d * sc * q - dmin * m; each block contributes d*sc*d_x*isum then
  *                -dmin*m*d_x*s, with isum = sum q*x exact and s the activation block sum.
+ *     STRATA_Q5K (the pages' 5-bit super-block type, 180 bytes per 256 weights; cols % 256 == 0):
+ *                Q4K with codes q in 0..31. Row r of the code plane (20*nb bytes at r*nb*20) holds
+ *                the row's nb nibble blocks (16 bytes each, as Q4: low 4 bits of element j in the low
+ *                nibble of byte j, of element j+16 in the high nibble), then nb 32-bit little-endian
+ *                words of fifth bits: bit 8k + g of block b's word is the fifth bit of element 4g+k
+ *                (g < 4) or 16+4(g-4)+k (g >= 4). The (sc, m) plane and the (d, dmin) plane follow
+ *                as in Q4K; w = d * sc * q - dmin * m, with the same two terms per block.
  *   The block-dot hook (strata_block_dots) returns isum as defined per format: Q4 sum (q-8)x, Q8
- *   sum qx, Q6 s0*sum16 + s1*sum16, Q4K sum qx.
+ *   sum qx, Q6 s0*sum16 + s1*sum16, Q4K and Q5K sum qx.
  *
  * Quantized activations (q8_1-style, one scale and one sum per 32 values), for n rows of `cols`:
  *     xq int8  [n][cols]   codes q in -127..127
@@ -95,7 +102,7 @@ extern "C" {
 
 #define STRATA_MAX_T 8             /* verify windows hold 1..8 tokens */
 
-typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1, STRATA_Q6 = 2, STRATA_Q4K = 3 } strata_fmt;
+typedef enum { STRATA_Q4 = 0, STRATA_Q8 = 1, STRATA_Q6 = 2, STRATA_Q4K = 3, STRATA_Q5K = 4 } strata_fmt;
 
 /* Static text for a status code (never NULL). */
 const char* strata_error_string(int status);
@@ -124,7 +131,7 @@ int strata_quantize_act(const float* x, int64_t n_rows, int64_t cols,
  *   W  : weight matrix [rows][cols] in `fmt` (layout above), 16-byte aligned.
  *   xq, xd, xs : quantized activations of T rows of `cols` (xq 16-byte aligned).
  *   y  : fp32 [T][rows] (token-major, rows contiguous), 4-byte aligned.
- *   1 <= T <= 8, rows >= 1, cols % 32 == 0 (cols % 256 == 0 for STRATA_Q6 and STRATA_Q4K),
+ *   1 <= T <= 8, rows >= 1, cols % 32 == 0 (cols % 256 == 0 for STRATA_Q6, STRATA_Q4K and STRATA_Q5K),
  *   32 <= cols <= 65536, T*cols <= 131072, and the staged activations (T*cols*1.25 bytes, a little
  *   more for Q6) plus one four-row slot of W must fit in shared memory (for example Q8 with cols
  *   16384 at T = 8 does not): otherwise STRATA_ERR_SHAPE.

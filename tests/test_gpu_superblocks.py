@@ -1,6 +1,7 @@
 """GPU parity of the 256-weight super-block formats through the same GEMV family: Q6 (6-bit codes,
-int8 sub-scale per 16 weights, fp16 d per 256) and Q4K (4-bit codes, 6-bit scale and minimum per 32
-weights, fp16 d and dmin per 256). Bars: exact integer dots (bit for bit), outputs within the fp32
+int8 sub-scale per 16 weights, fp16 d per 256), Q4K (4-bit codes, 6-bit scale and minimum per 32
+weights, fp16 d and dmin per 256) and Q5K (Q4K with 5-bit codes, the fifth bits in a per-block word
+after the row's nibble blocks). Bars: exact integer dots (bit for bit), outputs within the fp32
 bound of the oracle, every column of a T-token launch bitwise equal to the T = 1 launch, grouped
 launches equal to single calls.
 """
@@ -12,7 +13,7 @@ import oracle
 from block_quantized_token_strata_gb300 import strata, synth
 
 pytestmark = pytest.mark.gpu
-FMTS = [synth.Q6, synth.Q4K]
+FMTS = [synth.Q6, synth.Q4K, synth.Q5K]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -102,7 +103,7 @@ def test_q6_grouped_equals_separate_calls(Q6):
 def test_superblock_formats_reject_partial_superblocks():
     L = strata.lib()
     A16 = 0x10000
-    for fmt, per256 in ((synth.Q6, 210), (synth.Q4K, 148)):
+    for fmt, per256 in ((synth.Q6, 210), (synth.Q4K, 148), (synth.Q5K, 180)):
         assert L.strata_mmvq_multi(A16, 64, 288, fmt, A16, A16, A16, 1, A16, None) == -2   # 288 % 256 != 0
         assert L.strata_weight_bytes(10, 512, fmt) == 10 * 2 * per256
 
@@ -121,3 +122,25 @@ def test_q4k_head_argmax_matches_oracle():
         top = np.sort(lg_or[t])[-2:]
         if top[1] - top[0] > 2 * oracle.tolerance(A[t]).max():
             assert ids[t] == ids_or[t]
+
+
+def test_q5k_head_argmax_and_fifth_bits_matter():
+    """A Q5K head: ids and logits against the oracle; and the same codes with every fifth bit cleared
+    give different logits, so the kernel reads the fifth-bit words."""
+    vocab, cols, T = 6000, 2048, 3
+    w = synth.make_weights(vocab, cols, synth.Q5K, "q5khead")
+    xq, xd, xs = oracle.quantize_act(synth.make_activations(T, cols, "q5khead"))
+    lg = torch.empty((T, vocab), dtype=torch.float32, device="cuda")
+    ids = strata.head_argmax(cu(w.buf), vocab, cols, synth.Q5K, cu(xq), cu(xd), cu(xs), T, logits=lg).cpu().numpy()
+    ids_or, lg_or, A = oracle.head_argmax(w.buf, vocab, cols, synth.Q5K, xq, xd)
+    assert_within(lg.cpu().numpy(), lg_or, A, "q5k head")
+    for t in range(T):
+        assert ids[t] == int(np.argmax(lg.cpu().numpy()[t]))
+    cleared = w.buf.copy()
+    nb = cols // 32
+    for r in range(vocab):  # zero the row's fifth-bit words
+        cleared[r * nb * 20 + nb * 16: (r + 1) * nb * 20] = 0
+    y0 = strata.mmvq_multi(cu(cleared), vocab, cols, synth.Q5K, cu(xq), cu(xd), cu(xs), T).cpu().numpy()
+    y0_or, A0 = oracle.mmvq(cleared, vocab, cols, synth.Q5K, xq, xd)
+    assert_within(y0, y0_or, A0, "q5k without fifth bits")
+    assert (np.abs(y0 - lg.cpu().numpy()) > oracle.tolerance(A)).mean() > 0.5
