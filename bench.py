@@ -315,7 +315,7 @@ def main():
                          "hbm_frac": gbs / hbm_peak}
 
     # --- roofline of the dominant kernel: the grouped layer GEMV launch. The same launches as the
-    # step, captured as two graphs (layers = quantize per width + grouped GEMV; head) so that CUDA
+    # step, captured as two graphs (layers = one quantize launch + grouped GEMV; head) so that CUDA
     # events on the launching stream bracket each part.
     win = wins[T]
     g_lay, g_head = win.capture("layers"), win.capture("head")
@@ -342,7 +342,7 @@ def main():
                 "kernel": "gemv_kernel<Q4,T,grouped>: one launch streams all 192 layer matrices",
                 "bytes_per_launch": layer_bytes, "us_per_launch": lay_ms * 1e3,
                 "peak_kind": peak_kind,
-                "note": "time of the layer section = 3 quantize launches + the grouped GEMV launch",
+                "note": "time of the layer section = the quantize launch + the grouped GEMV launch",
                 "head": {"gbs": head_bytes / (head_ms * 1e-3) / 1e9, "us": head_ms * 1e3,
                          "frac": head_bytes / (head_ms * 1e-3) / 1e9 / hbm_peak}}
 
@@ -432,7 +432,7 @@ def main():
             "config": {"workload": WORKLOAD, "T": T, "layers": args.layers,
                        "weight_bytes_per_window": wts.weight_bytes,
                        "l2": "inputs larger than L2 (1.52 GB of weights per step)",
-                       "graph": "one CUDA graph per window: quantize per input width, one grouped GEMV "
+                       "graph": "one CUDA graph per window: one quantize launch over every input, one grouped GEMV "
                                 "launch over the 192 layer matrices, head GEMV + argmax"},
             "weight_gbs": wts.weight_bytes / (ms * 1e-3) / 1e9 * world,
             "hbm_frac": wts.weight_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
@@ -585,7 +585,7 @@ def run_case(args):
     if args.case == "gemm":  # the dense prompt GEMM
         print(json.dumps({"case": "gemm", **bench_prompt_gemm(torch, strata, synth, reps=args.reps)}))
         return
-    if args.case == "layers":  # the window's grouped layer launch (quantize per width + one GEMV launch)
+    if args.case == "layers":  # the window's grouped layer launch (one quantize launch + one GEMV launch)
         from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
         wts = WindowWeights(layers=args.layers, device="cuda", layer_fmt=args.fmt)
         win = VerifyWindow(wts, T)

@@ -5,9 +5,10 @@ down) Q4 projections, then the Q8 head GEMV with its per-token argmax. The layer
 (there is no model between them): each projection has its own seeded fp32 input. Two launch
 structures are provided:
 
-  * "grouped" (the step the benchmark times): the inputs are quantized once per input width (three
-    launches), all 192 layer GEMVs run as ONE grouped launch (strata_mmvq_grouped: the matrices
-    stream back to back, every SM busy), then the head GEMV + argmax;
+  * "grouped" (the step the benchmark times): every input is quantized by ONE launch (inputs, codes,
+    scales and sums are each one flat buffer in the same block order), all 192 layer GEMVs run as
+    ONE grouped launch (strata_mmvq_grouped: the matrices stream back to back, every SM busy), then
+    the head GEMV + argmax;
   * "chained": one quantize + one GEMV launch per projection, each kernel ordered after the one
     before it — the launch structure a chained model would need — kept for comparison.
 
@@ -47,20 +48,25 @@ class VerifyWindow:
         self.wts, self.T, self.mode, self.key = weights, T, mode, key
         self.shapes = weights.shapes
         n = len(self.shapes)
-        # inputs grouped by width, so that each width is quantized by one launch
+        # inputs grouped by width; x and its quantized codes, scales and sums are each one flat buffer
+        # in the same block order, so one quantize launch covers every input of the window (the
+        # quantizer works on each 32-value block alone, whatever the row length)
         self.widths = sorted({c for _, _, c, _ in self.shapes})
         members = {c: [i for i, s in enumerate(self.shapes) if s[2] == c] for c in self.widths}
         total = sum(T * c for _, _, c, _ in self.shapes)
         self.x_flat = torch.empty(total, dtype=torch.float32, device=device)
+        self.q_flat = torch.empty(total, dtype=torch.int8, device=device)
+        self.d_flat = torch.empty(total // 32, dtype=torch.float32, device=device)
+        self.s_flat = torch.empty(total // 32, dtype=torch.int32, device=device)
         self.offset = [0] * n          # element offset of each projection's input in x_flat
         self.gx, self.gq, self.gd, self.gs = {}, {}, {}, {}
         off = 0
         for c in self.widths:
             k = len(members[c])
             self.gx[c] = self.x_flat[off: off + k * T * c].view(k * T, c)
-            self.gq[c] = torch.empty((k * T, c), dtype=torch.int8, device=device)
-            self.gd[c] = torch.empty((k * T, c // 32), dtype=torch.float32, device=device)
-            self.gs[c] = torch.empty((k * T, c // 32), dtype=torch.int32, device=device)
+            self.gq[c] = self.q_flat[off: off + k * T * c].view(k * T, c)
+            self.gd[c] = self.d_flat[off // 32: (off + k * T * c) // 32].view(k * T, c // 32)
+            self.gs[c] = self.s_flat[off // 32: (off + k * T * c) // 32].view(k * T, c // 32)
             for j, i in enumerate(members[c]):
                 self.offset[i] = off + j * T * c
             off += k * T * c
@@ -101,7 +107,7 @@ class VerifyWindow:
     # ---- launches ----
     def launches_per_step(self) -> int:
         if self.mode == "grouped":
-            return len(self.widths) + 1 + 2     # quantize per width, grouped GEMV, head + finalize
+            return 1 + 1 + 2                    # one quantize, grouped GEMV, head + finalize
         return 2 * (len(self.shapes) - 1) + 3   # quantize + GEMV per layer matrix; quantize + head + finalize
 
     def enqueue(self, stream=None, part: str = "all") -> None:
@@ -110,8 +116,8 @@ class VerifyWindow:
         name, vocab, hcols, hfmt = self.shapes[-1]
         if self.mode == "grouped":
             if part in ("all", "layers"):
-                for c in self.widths:
-                    strata.quantize_act(self.gx[c], self.gq[c], self.gd[c], self.gs[c], stream=stream)
+                strata.quantize_act(self.x_flat.view(1, -1), self.q_flat.view(1, -1), self.d_flat.view(1, -1),
+                                    self.s_flat.view(1, -1), stream=stream)
                 strata.mmvq_grouped(self.descs, self.wts.layer_fmt, self.T, stream=stream)
         else:
             if part in ("all", "layers"):

@@ -1,5 +1,5 @@
 """The full verify window at its real size, in the launch configurations the benchmark times (one
-CUDA graph per window: grouped = quantize per width + one grouped GEMV launch + head; chained =
+CUDA graph per window: grouped = one quantize launch + one grouped GEMV launch + head; chained =
 quantize + GEMV per projection + head), against the oracle: every matrix on sampled rows, the
 head's argmax on all tokens; graph replay bitwise equal to eager launches; both launch structures
 bitwise equal to each other; T = 4 columns bitwise equal to T = 1."""
