@@ -106,20 +106,24 @@ static int q6_subscale(const uint8_t* W, int64_t rows, int64_t nb, int64_t r, in
 }
 
 /* weight code of element j (0..31) of block (r, b), already offset: Q4 q-8, Q8 q */
+/* Q5K code of element j (0..31) of block (r, b): the row's nibble blocks, then its fifth-bit words;
+ * code = low nibble | fifth bit << 4 */
+__attribute__((noinline)) static int q5k_code(const uint8_t* W, int64_t nb, int64_t r, int64_t b, int j)
+{
+    const uint8_t* row = W + r * nb * 20;
+    int byte = row[16 * b + (j & 15)];
+    int low = (j < 16) ? (byte & 0x0F) : (byte >> 4);
+    const uint8_t* hw = row + 16 * nb + 4 * b;
+    uint32_t bits = (uint32_t)hw[0] | ((uint32_t)hw[1] << 8) | ((uint32_t)hw[2] << 16) | ((uint32_t)hw[3] << 24);
+    int group = (j < 16) ? j / 4 : 4 + (j - 16) / 4;
+    int k = j % 4;
+    int fifth = (int)((bits >> (8 * k + group)) & 1u);
+    return low | (fifth << 4);
+}
+
 static int weight_code(const uint8_t* W, int64_t nb, int fmt, int64_t r, int64_t b, int j)
 {
-    if (fmt == OR_Q5K) {
-        /* the row's nibble blocks, then its fifth-bit words; code = low nibble | fifth bit << 4 */
-        const uint8_t* row = W + r * nb * 20;
-        int byte = row[16 * b + (j & 15)];
-        int low = (j < 16) ? (byte & 0x0F) : (byte >> 4);
-        const uint8_t* hw = row + 16 * nb + 4 * b;
-        uint32_t bits = (uint32_t)hw[0] | ((uint32_t)hw[1] << 8) | ((uint32_t)hw[2] << 16) | ((uint32_t)hw[3] << 24);
-        int group = (j < 16) ? j / 4 : 4 + (j - 16) / 4;
-        int k = j % 4;
-        int fifth = (int)((bits >> (8 * k + group)) & 1u);
-        return low | (fifth << 4);
-    }
+    if (fmt == OR_Q5K) return q5k_code(W, nb, r, b, j);
     const uint8_t* blk = W + (r * nb + b) * qbytes(fmt);
     if (fmt == OR_Q4 || fmt == OR_Q4K) {  /* Q4K codes carry no offset: its minimum does that */
         int byte = blk[j & 15];
