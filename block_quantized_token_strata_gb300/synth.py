@@ -125,7 +125,7 @@ def make_q5k_buffer(q: np.ndarray, sc: np.ndarray, mn: np.ndarray, d: np.ndarray
 
 
 def make_weights(rows: int, cols: int, fmt: int, *key) -> Weights:
-    """A seeded [rows][cols] matrix in Q4, Q8 or Q6 (planar layout, see include/strata.h)."""
+    """A seeded [rows][cols] matrix in Q4, Q8, Q6, Q4K or Q5K (planar layout, see include/strata.h)."""
     if cols % QK or rows <= 0:
         raise ValueError("cols must be a multiple of 32 and rows positive")
     rng = _rng("weights", rows, cols, fmt, *key)

@@ -181,7 +181,7 @@ int strata_device_error(int* out, int clear);
  *   Source: verify.hpp, Verifier::run (argmax after each token) and `h_out_/m_out_`, `copy_logits`;
  *   tie rule from dsv41-offload worker/tp2.py, EmuComm.argmax and markov_local_argmax
  *   ("ties -> lowest"): among equal maximal logits the lowest vocabulary id wins.
- *   W : [vocab][cols] in `fmt` (Q8 in the verify configuration; Q4 is accepted too).
+ *   W : [vocab][cols] in `fmt` (Q8 in the verify configuration; Q4, Q6, Q4K and Q5K are accepted too).
  *   ids : int32 [T] device output.  logits : fp32 [T][vocab] or NULL (then not written).
  *   workspace : device scratch of strata_head_argmax_workspace(vocab, T) bytes, 16-byte aligned;
  *   its contents need no initialisation and are dead after the call.
@@ -220,7 +220,8 @@ int strata_head_argmax_margin(const void* W, int64_t vocab, int64_t cols, int fm
  *   It allocates nothing and calls no allocating routine. Its first call on a device looks up the
  *   array's device address (make that first call before any stream capture). All calls share the
  *   array: calls that overlap on the GPU race on it. Returns STRATA_ERR_WORKSPACE when a launch
- *   would need more than the 64 KiB; otherwise the errors of strata_head_argmax.
+ *   would need more than the 64 KiB; otherwise the errors of strata_head_argmax. Formats: Q4 and Q8
+ *   only (others are STRATA_ERR_FMT).
  */
 int strata_head_argmax_noalloc(const void* W, int64_t vocab, int64_t cols, int fmt,
                                const int8_t* xq, const float* xd, const int32_t* xs, int T,
