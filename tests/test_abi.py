@@ -39,6 +39,9 @@ def test_error_strings(L):
     assert L.strata_error_string(-99) == b"unknown status"
 
 
+A16 = 0x10000  # fake, aligned, never dereferenced: every call below fails its host checks first
+
+
 def test_weight_bytes(L):
     assert L.strata_weight_bytes(4096, 4096, 0) == 4096 * 128 * 18
     assert L.strata_weight_bytes(151936, 2048, 1) == 151936 * 64 * 34
@@ -46,7 +49,18 @@ def test_weight_bytes(L):
     assert L.strata_weight_bytes(4, 64, 9) == 0
 
 
-A16 = 0x10000  # fake, aligned, never dereferenced: every call below fails its host checks first
+
+@pytest.mark.parametrize("fmt,per256", [(2, 210), (3, 148), (4, 180)])
+def test_superblock_formats_host_checks(L, fmt, per256):
+    """Q6 / Q4K / Q5K: bytes per 256 weights, whole super-blocks only (checked before any launch),
+    and the no-alloc head takes Q4 and Q8 only."""
+    assert L.strata_weight_bytes(10, 512, fmt) == 10 * 2 * per256
+    assert L.strata_weight_bytes(10, 288, fmt) == 0                        # 288 % 256 != 0
+    assert L.strata_mmvq_multi(A16, 64, 288, fmt, A16, A16, A16, 1, A16, None) == -2
+    assert L.strata_mmvq_multi(A16, 64, 512, fmt, A16, A16, A16, 9, A16, None) == -3
+    assert L.strata_head_argmax_noalloc(A16, 64, 512, fmt, A16, A16, A16, 1, A16, None, None) == -4
+
+
 
 
 @pytest.mark.parametrize("args,code", [
