@@ -495,3 +495,21 @@ def test_q5k_brute_force_dense(orc):
     assert np.array_equal(isum.reshape(T, rows, cols // 32), want)
     from block_quantized_token_strata_gb300 import synth
     assert np.array_equal(synth.make_q5k_buffer(q, sc, mn, d, dmin), W)
+
+
+def test_quantizer_is_blockwise_so_inputs_concatenate(orc):
+    """The quantizer sees one 32-value block at a time: quantizing inputs of different widths laid
+    end to end as one row gives each input's own codes, scales and sums (the window quantizes all
+    of its inputs in one call on this property)."""
+    rng = np.random.default_rng(41)
+    parts = [rng.standard_normal((4, c)).astype(np.float32) * s for c, s in ((2048, 1.0), (4096, 3.0), (96, 0.01))]
+    parts[1][0, :32] = 0.0                                       # an all-zero block inside the row
+    flat = np.concatenate([p.reshape(-1) for p in parts])[None, :]
+    qf, df, sf = orc.quantize_act(flat)
+    qs, ds, ss = [], [], []
+    for p in parts:
+        q, d, s = orc.quantize_act(p)
+        qs.append(q.reshape(-1)); ds.append(d.reshape(-1)); ss.append(s.reshape(-1))
+    assert np.array_equal(qf[0], np.concatenate(qs))
+    assert np.array_equal(df[0].view(np.uint32), np.concatenate(ds).view(np.uint32))
+    assert np.array_equal(sf[0], np.concatenate(ss))
