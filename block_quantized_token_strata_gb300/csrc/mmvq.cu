@@ -378,9 +378,11 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 pdl_wait();
                 pdl_launch();
             }
-            // no copy may still be landing in shared memory when the CTA leaves
+            // no copy may still be landing in shared memory when the CTA leaves: the issued copies are
+            // waited for (bounded) even after an abort
+            const int no_abort = 0;
             for (int i = (k > NST ? k - NST : 0); i < k; ++i)
-                if (!mbar_wait(smem_u32(&bars[i % NST]), (i / NST) & 1, &s_abort)) {
+                if (!mbar_wait(smem_u32(&bars[i % NST]), (i / NST) & 1, &no_abort)) {
                     atomicOr(&g_strata_device_error, 1 | 8);
                     break;
                 }
