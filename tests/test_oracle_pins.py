@@ -513,3 +513,43 @@ def test_quantizer_is_blockwise_so_inputs_concatenate(orc):
     assert np.array_equal(qf[0], np.concatenate(qs))
     assert np.array_equal(df[0].view(np.uint32), np.concatenate(ds).view(np.uint32))
     assert np.array_equal(sf[0], np.concatenate(ss))
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 4])
+def test_superblock_tolerance_mass_is_sum_of_abs_terms(orc, fmt):
+    """A (the tolerance's mass) is the sum of |term| over the format's terms, computed here from the
+    unpacked fields: Q6 one term per 16 weights (d*s*d_x*isum16), Q4K / Q5K two per block
+    (d*sc*d_x*isum and -dmin*m*d_x*sum x). A too-large A would loosen every GPU comparison."""
+    rng = np.random.default_rng(53 + fmt)
+    rows, cols, T = 3, 512, 2
+    nb = cols // 32
+    xq, xd, _ = orc.quantize_act(rng.standard_normal((T, cols)).astype(np.float32))
+    x = xq.astype(np.int64).reshape(T, nb, 32)
+    dx = xd.astype(np.float64)
+    if fmt == 2:
+        q = rng.integers(0, 64, size=(rows, cols)).astype(np.uint8)
+        sub = rng.integers(-127, 128, size=(rows, cols // 16)).astype(np.int8)
+        d = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+        W = pack_q6(q, sub, d)
+        qq = q.astype(np.int64).reshape(rows, nb, 2, 16) - 32
+        isum16 = np.einsum("rbhj,tbhj->trbh", qq, x.reshape(T, nb, 2, 16))
+        terms = (d.astype(np.float64).repeat(8, axis=1)[None, :, :, None] * sub.astype(np.float64).reshape(rows, nb, 2)[None]
+                 * dx[:, None, :, None] * isum16)
+    else:
+        hi = 32 if fmt == 4 else 16
+        q = rng.integers(0, hi, size=(rows, cols)).astype(np.uint8)
+        sc = rng.integers(0, 64, size=(rows, nb)).astype(np.uint8)
+        mn = rng.integers(0, 64, size=(rows, nb)).astype(np.uint8)
+        d = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+        dmin = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
+        W = (pack_q5k if fmt == 4 else pack_q4k)(q, sc, mn, d, dmin)
+        isum = np.einsum("rbj,tbj->trb", q.astype(np.int64).reshape(rows, nb, 32), x)
+        xsum = x.sum(axis=2)                                                   # [T][nb]
+        t1 = d.astype(np.float64).repeat(8, axis=1)[None] * sc.astype(np.float64)[None] * dx[:, None, :] * isum
+        t2 = -dmin.astype(np.float64).repeat(8, axis=1)[None] * mn.astype(np.float64)[None] * dx[:, None, :] * xsum[:, None, :]
+        terms = np.stack([t1, t2], axis=-1)
+    y, A = orc.mmvq(W, rows, cols, fmt, xq, xd)
+    want_A = np.abs(terms).reshape(T, rows, -1).sum(axis=2)
+    want_y = terms.reshape(T, rows, -1).sum(axis=2)
+    assert np.allclose(A, want_A, rtol=1e-12, atol=0)
+    assert np.allclose(y, want_y, rtol=1e-12, atol=1e-12 * np.abs(want_y).max())
