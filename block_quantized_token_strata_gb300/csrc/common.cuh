@@ -79,21 +79,29 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for phase `parity`, bounded: gives up (returns false) after about two seconds of wall time,
-// after an iteration cap as a backstop, or as soon as *abort becomes non-zero. The caller then
-// flags the error and leaves without touching the data the barrier guards.
+// Wait for phase `parity`, bounded: gives up (returns false) after `limit_ns` of wall time (two
+// seconds unless a caller asks for less), after an iteration cap as a backstop, or as soon as *abort
+// becomes non-zero. The caller then flags the error and leaves without touching the data the
+// barrier guards.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kWaitIterCap = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < kWaitIterCap; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
+
+// The device error word of the bounded waits (bit 0: a wait ran out; higher bits name the wait).
+// The library is built without relocatable device code, so every translation unit that includes
+// this header holds its own copy; each unit whose kernels set it exports a host reader (internal.h)
+// and strata_device_error combines them.
+static __device__ int g_strata_device_error = 0;
 // generic-proxy shared-memory writes before later async-proxy (TMA) accesses of the same bytes
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

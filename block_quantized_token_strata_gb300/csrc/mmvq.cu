@@ -87,9 +87,8 @@ constexpr int kMaxGroup = 192;            // matrices per grouped launch
 constexpr int kMaxGrid = 1024;
 constexpr int kCtasPerSm = 1;             // resident CTAs per SM the launch plans for
 
-// bit 0: a bounded wait ran out; bit 1: the producer waiting for a free stage; bit 2: a consumer
-// waiting for a stage's bytes; bit 3: the producer draining its last copies
-__device__ int g_strata_device_error = 0;
+// Device error word bits set here: bit 0 a bounded wait ran out; bit 1 the producer waiting for a
+// free stage; bit 2 a consumer waiting for a stage's bytes; bit 3 the producer draining its last copies.
 
 template <int FMT> struct FmtInfo;
 template <> struct FmtInfo<0> { static constexpr int kQB = 16; };  // Q4: 16 code bytes per block
@@ -1152,12 +1151,23 @@ cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt
     return launch_pdl(block_dots_kernel<1>, dim3(grid), dim3(256), 0, stream, w, int(rows), nb, xq, xs, T, isum);
 }
 
-cudaError_t read_device_error(int* out, bool clear)
+cudaError_t read_device_error_gemv(int* out, bool clear)
 {
     cudaError_t e = cudaMemcpyFromSymbol(out, g_strata_device_error, sizeof(int));
     if (e != cudaSuccess || !clear) return e;
     const int zero = 0;
     return cudaMemcpyToSymbol(g_strata_device_error, &zero, sizeof(int));
+}
+
+// the word as the C ABI reports it: the copies of every translation unit whose kernels set it, ORed
+cudaError_t read_device_error(int* out, bool clear)
+{
+    int a = 0, b = 0, c = 0;
+    cudaError_t e = read_device_error_gemv(&a, clear);
+    if (e == cudaSuccess) e = read_device_error_moe(&b, clear);
+    if (e == cudaSuccess) e = read_device_error_probe(&c, clear);
+    *out = a | b | c;
+    return e;
 }
 
 }  // namespace strata
