@@ -129,6 +129,7 @@ static int head_call(const void* W, int64_t vocab, int64_t cols, int fmt, const 
     if (st != STRATA_OK) return st;
     st = check_matrix(vocab, cols, fmt);
     if (st != STRATA_OK) return st;
+    if (vocab >= kHeadMaxVocab) return STRATA_ERR_SHAPE;
     if (T < 1 || T > STRATA_MAX_T) return STRATA_ERR_T;
     if (int64_t(T) * cols > kMaxStagedTCols || !gemv_shape_fits(cols, fmt, T)) return STRATA_ERR_SHAPE;
     if (!aligned(W, 16) || !aligned(ids, 4) || (logits && !aligned(logits, 4)) || (margin && !aligned(margin, 4)))
@@ -196,9 +197,9 @@ int strata_moe_debug_views(int n_expert, int64_t n_tok, int k, int64_t hidden, i
     return STRATA_OK;
 }
 
-int strata_moe_grouped(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
-                       const int32_t* ids, int64_t n_tok, int k, const float* x, float* y, void* workspace,
-                       size_t ws_bytes, int32_t* err_word, cudaStream_t stream)
+static int moe_call(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
+                    const int32_t* ids, int64_t n_tok, int k, const float* x, float* y, void* workspace,
+                    size_t ws_bytes, int32_t* err_word, float* gu, cudaStream_t stream)
 {
     if (!experts || !ids || !x || !y) return STRATA_ERR_NULL;
     if (n_expert < 1 || n_tok < 1 || k < 1 || k > 16) return STRATA_ERR_SHAPE;
@@ -206,11 +207,35 @@ int strata_moe_grouped(const strata_expert* experts, int n_expert, int64_t hidde
     if (hidden > 16384 || inter > 16384 || n_tok * k > (int64_t(1) << 30)) return STRATA_ERR_SHAPE;
     if (!aligned(experts, 8) || !aligned(ids, 4) || !aligned(x, 16) || !aligned(y, 16)) return STRATA_ERR_ALIGN;
     if (err_word && !aligned(err_word, 4)) return STRATA_ERR_ALIGN;
+    if (gu && !aligned(gu, 16)) return STRATA_ERR_ALIGN;
     const MoeLayout L = moe_workspace_layout(n_expert, n_tok, k, hidden, inter);
     if (!workspace || ws_bytes < L.total) return STRATA_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return STRATA_ERR_ALIGN;
     return cuda_status(launch_moe_grouped(experts, n_expert, hidden, inter, ids, n_tok, k, x, y,
-                                          static_cast<uint8_t*>(workspace), L, err_word, stream));
+                                          static_cast<uint8_t*>(workspace), L, err_word, gu, stream));
+}
+
+int strata_moe_grouped(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
+                       const int32_t* ids, int64_t n_tok, int k, const float* x, float* y, void* workspace,
+                       size_t ws_bytes, int32_t* err_word, cudaStream_t stream)
+{
+    return moe_call(experts, n_expert, hidden, inter, ids, n_tok, k, x, y, workspace, ws_bytes, err_word,
+                    nullptr, stream);
+}
+
+int strata_moe_grouped_gu(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
+                          const int32_t* ids, int64_t n_tok, int k, const float* x, float* y, void* workspace,
+                          size_t ws_bytes, int32_t* err_word, float* gu, cudaStream_t stream)
+{
+    if (!gu) return STRATA_ERR_NULL;
+    return moe_call(experts, n_expert, hidden, inter, ids, n_tok, k, x, y, workspace, ws_bytes, err_word, gu,
+                    stream);
+}
+
+int strata_wait_probe(int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream)
+{
+    if (limit_ns < 1 || limit_ns > 1000000000 || abort_after_ns > 1000000000) return STRATA_ERR_SHAPE;
+    return cuda_status(launch_wait_probe(limit_ns, abort_after_ns < 0 ? -1 : abort_after_ns, stream));
 }
 
 }  // extern "C"

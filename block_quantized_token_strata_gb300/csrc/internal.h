@@ -50,14 +50,22 @@ constexpr int kMaxGroupedMatrices = 192;
 int gemv_warps_per_row(int64_t cols, int fmt);
 // whether the shared-memory plan of a shape fits at T
 bool gemv_shape_fits(int64_t cols, int fmt, int T);
-// device error word: bit 0 = a bounded wait in a kernel ran out
+// device error word: bit 0 = a bounded wait in a kernel ran out (the OR of every unit's copy)
 cudaError_t read_device_error(int* out, bool clear);
+cudaError_t read_device_error_gemv(int* out, bool clear);
+cudaError_t read_device_error_moe(int* out, bool clear);
+cudaError_t read_device_error_probe(int* out, bool clear);
+// test hook: one CTA waits, bounded by limit_ns, on an mbarrier nobody arrives at (abort_after_ns
+// >= 0: a second warp raises the CTA's abort flag after that long instead)
+cudaError_t launch_wait_probe(int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream);
 
 cudaError_t launch_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq,
                               const int32_t* xs, int T, int32_t* isum, cudaStream_t stream);
 
 // largest T * cols the GEMV kernels stage in shared memory
 constexpr int64_t kMaxStagedTCols = 131072;
+// the head's per-lane candidates carry the token in bits 27-29 of the row id, so vocab < 2^27
+constexpr int64_t kHeadMaxVocab = int64_t(1) << 27;
 
 // ---- prompt-chunk MoE ----------------------------------------------------------------------------
 // Byte offsets of the sections of a strata_moe_grouped workspace (each 256-byte aligned).
@@ -71,9 +79,11 @@ struct MoeLayout {
 MoeLayout moe_workspace_layout(int n_expert, int64_t n_tok, int k, int64_t hidden, int64_t inter);
 
 struct ExpertPtrs;  // device-side view of strata_expert (three const void*)
+// gu (may be null): fp32 [n_tok*k][2][inter], the gate then the up outputs of every valid pair
 cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden, int64_t inter,
                                const int32_t* ids, int64_t n_tok, int k, const float* x, float* y,
-                               uint8_t* ws, const MoeLayout& L, int32_t* err_word, cudaStream_t stream);
+                               uint8_t* ws, const MoeLayout& L, int32_t* err_word, float* gu,
+                               cudaStream_t stream);
 cudaError_t launch_prompt_gemm(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
                                int64_t n_tok, float* y, cudaStream_t stream);
 

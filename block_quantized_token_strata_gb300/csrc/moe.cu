@@ -144,7 +144,6 @@ constexpr int kTcOffRaw = kTcOffScale + kTcScale * 1024;
 constexpr int kTcOffBars = kTcOffRaw + kTcRaw * kTcRawSlot;
 constexpr int kTcSmem = kTcOffBars + 512;
 
-extern __device__ int g_strata_device_error;
 
 struct MoeTcArgs {
     const ExpertPtrs* experts;
@@ -159,6 +158,7 @@ struct MoeTcArgs {
     float* hd;
     int32_t* hs;
     float* y;
+    float* gu;                 // test hook (null in the product call): fp32 [n_pair][2][inter], g then u by pair
     // dense prompt GEMM (down-phase kernel only): the one Q4 matrix [hidden][inter] and the number of
     // activation rows; tiles then cover rows 0.. in order and row m of the output is y row m
     const uint8_t* dense_w;
@@ -489,6 +489,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
                 for (int q = 0; q < 32; ++q) unpack_f2(acc2[q], acc[2 * q], acc[2 * q + 1]);
                 const int P = tile.m0 + m;
                 if (PHASE == 0) {
+                    if (a.gu != nullptr) {  // the fp32 gate and up outputs of this pair, as computed
+                        float* gd = a.gu + size_t(__ldg(a.pairs + P)) * 2 * a.inter + tile.nt * 64 + 32 * cg;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            reinterpret_cast<float4*>(gd)[j] =
+                                make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                            reinterpret_cast<float4*>(gd + a.inter)[j] =
+                                make_float4(acc[32 + 4 * j], acc[33 + 4 * j], acc[34 + 4 * j], acc[35 + 4 * j]);
+                        }
+                    }
                     // h = silu(g) * u for the 32 inter columns nt*64 + 32*cg + j, then one quant block
                     float h[32];
                     float amax = 0.0f;
@@ -541,6 +551,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
     }
 }
 
+cudaError_t read_device_error_moe(int* out, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_strata_device_error, sizeof(int));
+    if (e != cudaSuccess || !clear) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_strata_device_error, &zero, sizeof(int));
+}
+
 // running count of 128-row M-tiles per expert (one small CTA)
 __global__ void moe_tiles_kernel(const int32_t* __restrict__ counts, int n_expert, int32_t* __restrict__ mcum)
 {
@@ -558,7 +576,8 @@ __global__ void moe_tiles_kernel(const int32_t* __restrict__ counts, int n_exper
 
 cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden, int64_t inter,
                                const int32_t* ids, int64_t n_tok, int k, const float* x, float* y,
-                               uint8_t* ws, const MoeLayout& L, int32_t* err_word, cudaStream_t stream)
+                               uint8_t* ws, const MoeLayout& L, int32_t* err_word, float* gu,
+                               cudaStream_t stream)
 {
     const int n_pair = int(n_tok * k);
     int8_t* xq = reinterpret_cast<int8_t*>(ws + L.xq);
@@ -597,6 +616,7 @@ cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden
     a.hd = hd;
     a.hs = hs;
     a.y = y;
+    a.gu = gu;
     // persistent: one CTA per SM, or fewer when even the largest grouping has fewer tiles
     // (at most n_pair/128 + n_expert M-tiles)
     const int max_mtiles = (n_pair + 127) / 128 + n_expert;

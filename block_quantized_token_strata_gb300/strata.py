@@ -64,10 +64,13 @@ def lib() -> ctypes.CDLL:
             L.strata_head_argmax_noalloc.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P]
             L.strata_head_argmax_margin.argtypes = [P, I64, I64, I, P, P, P, I, P, P, P, P, SZ, P]
             L.strata_gemm_q4.argtypes = [P, I64, I64, P, P, I64, P, P]
+            L.strata_moe_grouped_gu.argtypes = [P, I, I64, I64, P, I64, I, P, P, P, SZ, P, P, P]
+            L.strata_wait_probe.argtypes = [I64, I64, P]
             for name in ("strata_quantize_act", "strata_mmvq_multi", "strata_head_argmax",
                          "strata_moe_grouped", "strata_moe_debug_views", "strata_block_dots",
                          "strata_mmvq_grouped", "strata_device_error", "strata_head_argmax_noalloc",
-                         "strata_head_argmax_margin", "strata_gemm_q4"):
+                         "strata_head_argmax_margin", "strata_gemm_q4", "strata_moe_grouped_gu",
+                         "strata_wait_probe"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -146,6 +149,11 @@ def device_error(clear: bool = True) -> int:
     return out.value
 
 
+def wait_probe(limit_ns: int, abort_after_ns: int = -1, stream=None) -> None:
+    """Enqueue the bounded-wait probe (a wait nothing completes; it must end by its limit or abort)."""
+    _check(lib().strata_wait_probe(int(limit_ns), int(abort_after_ns), _stream(stream)), "strata_wait_probe")
+
+
 def head_argmax_workspace(vocab: int, T: int) -> int:
     return int(lib().strata_head_argmax_workspace(vocab, T))
 
@@ -220,8 +228,9 @@ def expert_table(experts, device) -> torch.Tensor:
 
 
 def moe_grouped(expert_tab, n_expert: int, hidden: int, inter: int, ids, x, y=None, workspace=None,
-                err_word=None, stream=None):
-    """y fp32 [n_tok*k][hidden]: one row per (token, slot) pair, grouped expert GEMMs inside."""
+                err_word=None, stream=None, gu=None):
+    """y fp32 [n_tok*k][hidden]: one row per (token, slot) pair, grouped expert GEMMs inside. With
+    ``gu`` (fp32 [n_tok*k][2][inter]) the test-hook entry point also writes each pair's g and u."""
     n_tok, k = ids.shape
     dev = x.device
     if y is None:
@@ -230,7 +239,12 @@ def moe_grouped(expert_tab, n_expert: int, hidden: int, inter: int, ids, x, y=No
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else need
-    _check(lib().strata_moe_grouped(_ptr(expert_tab), n_expert, hidden, inter, _ptr(ids), n_tok, k, _ptr(x),
-                                    _ptr(y), _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream)),
-           "strata_moe_grouped")
+    if gu is None:
+        _check(lib().strata_moe_grouped(_ptr(expert_tab), n_expert, hidden, inter, _ptr(ids), n_tok, k, _ptr(x),
+                                        _ptr(y), _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream)),
+               "strata_moe_grouped")
+    else:
+        _check(lib().strata_moe_grouped_gu(_ptr(expert_tab), n_expert, hidden, inter, _ptr(ids), n_tok, k,
+                                           _ptr(x), _ptr(y), _ptr(workspace), ws_bytes, _ptr(err_word), _ptr(gu),
+                                           _stream(stream)), "strata_moe_grouped_gu")
     return y

@@ -170,11 +170,25 @@ int strata_mmvq_grouped(const strata_gemv_desc* descs, int n, int fmt, int T, cu
 
 /*
  * strata_device_error — the library's device error word, read synchronously (waits for the
- *   device). Bit 0: a bounded wait inside a kernel ran out (a bulk copy or a pipeline slot never
- *   completed); that kernel then skipped the rest of its work and left its outputs incomplete.
- *   clear != 0 resets the word. Returns STRATA_OK or STRATA_ERR_CUDA.
+ *   device). Bit 0: a bounded wait inside a kernel ran out (a bulk copy, a pipeline slot or a tensor
+ *   core accumulator never completed, or the kernel's abort flag was raised); that kernel then
+ *   skipped the rest of its work and left its outputs incomplete. Bits 1-4 name the wait: 1 the
+ *   GEMV producer waiting for a free stage, 2 a GEMV consumer waiting for a stage's bytes, 3 the
+ *   GEMV producer draining its last copies, 4 strata_wait_probe. Every kernel that can set it (GEMV,
+ *   head, MoE, prompt GEMM, the probe) is covered. clear != 0 resets the word. Returns STRATA_OK or
+ *   STRATA_ERR_CUDA. The error-word convention follows dsv41-offload worker/tp2.py (collectives set
+ *   bits in an error word instead of trapping; the host reads and clears it).
  */
 int strata_device_error(int* out, int clear);
+
+/*
+ * strata_wait_probe — test hook for the bounded device waits: one CTA waits on a pipeline barrier
+ *   that nothing ever completes, so the wait can only end by its time limit (limit_ns, 1..1e9) or,
+ *   when abort_after_ns >= 0 (at most 1e9), by a second warp raising the CTA's abort flag after that
+ *   long. Either way the kernel returns and sets bits 0 and 4 of the device error word; nothing else
+ *   is touched. Asynchronous on `stream`. Errors: SHAPE (limits out of range), CUDA.
+ */
+int strata_wait_probe(int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream);
 
 /*
  * strata_head_argmax — vocabulary head GEMV fused with the per-token argmax.
@@ -182,6 +196,8 @@ int strata_device_error(int* out, int clear);
  *   tie rule from dsv41-offload worker/tp2.py, EmuComm.argmax and markov_local_argmax
  *   ("ties -> lowest"): among equal maximal logits the lowest vocabulary id wins.
  *   W : [vocab][cols] in `fmt` (Q8 in the verify configuration; Q4, Q6, Q4K and Q5K are accepted too).
+ *   1 <= vocab < 2^27 (134,217,728): larger vocabularies are STRATA_ERR_SHAPE. The other shape rules
+ *   are strata_mmvq_multi's.
  *   ids : int32 [T] device output.  logits : fp32 [T][vocab] or NULL (then not written).
  *   workspace : device scratch of strata_head_argmax_workspace(vocab, T) bytes, 16-byte aligned;
  *   its contents need no initialisation and are dead after the call.
@@ -219,9 +235,11 @@ int strata_head_argmax_margin(const void* W, int64_t vocab, int64_t cols, int fm
  *   64 KiB array inside the library, held on every device that loads it until the process exits.
  *   It allocates nothing and calls no allocating routine. Its first call on a device looks up the
  *   array's device address (make that first call before any stream capture). All calls share the
- *   array: calls that overlap on the GPU race on it. Returns STRATA_ERR_WORKSPACE when a launch
- *   would need more than the 64 KiB; otherwise the errors of strata_head_argmax. Formats: Q4 and Q8
- *   only (others are STRATA_ERR_FMT).
+ *   array: calls that overlap on the GPU race on it. The address is looked up again in a new CUDA
+ *   context (after a device reset), so that first-call rule holds per context. Returns
+ *   STRATA_ERR_WORKSPACE when a launch would need more than the 64 KiB; otherwise the errors of
+ *   strata_head_argmax, with the same shape rules (vocab < 2^27; a shape whose staged activations do
+ *   not fit is STRATA_ERR_SHAPE). Formats: Q4 and Q8 only (others are STRATA_ERR_FMT).
  */
 int strata_head_argmax_noalloc(const void* W, int64_t vocab, int64_t cols, int fmt,
                                const int8_t* xq, const float* xd, const int32_t* xs, int T,
@@ -271,6 +289,17 @@ size_t strata_moe_grouped_workspace(int n_expert, int64_t n_tok, int k, int64_t 
 int strata_moe_grouped(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
                        const int32_t* ids, int64_t n_tok, int k, const float* x, float* y,
                        void* workspace, size_t ws_bytes, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * strata_moe_grouped_gu — test hook: strata_moe_grouped (same arguments, same kernels, same results)
+ *   that also writes the fp32 gate and up outputs g, u of every pair with a valid id, exactly as the
+ *   kernel holds them before SiLU: gu fp32 [n_tok*k][2][inter] (pair p = tok*k + slot; row p, plane 0
+ *   is g, plane 1 is u), device, 16-byte aligned. Rows of pairs with an out-of-range id are not
+ *   written. Errors: those of strata_moe_grouped; gu NULL is STRATA_ERR_NULL.
+ */
+int strata_moe_grouped_gu(const strata_expert* experts, int n_expert, int64_t hidden, int64_t inter,
+                          const int32_t* ids, int64_t n_tok, int k, const float* x, float* y,
+                          void* workspace, size_t ws_bytes, int32_t* err_word, float* gu, cudaStream_t stream);
 
 /*
  * strata_moe_debug_views — byte offsets, inside a strata_moe_grouped workspace, of the grouping

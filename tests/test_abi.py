@@ -138,3 +138,40 @@ def test_gemm_rejects(L):
     assert L.strata_gemm_q4(*a) == -7                 # xq alignment
     a = list(ok); a[6] = A16 + 4
     assert L.strata_gemm_q4(*a) == -7                 # y alignment
+
+
+def test_head_vocab_limit(L):
+    """The head keeps a candidate's token in bits 27-29 of its row id, so every head entry point
+    rejects vocab >= 2^27 on the host (before the workspace check, before any launch)."""
+    V = 1 << 27
+    big = 1 << 40
+    assert L.strata_head_argmax(A16, V, 2048, 1, A16, A16, A16, 4, A16, None, A16, big, None) == -2
+    assert L.strata_head_argmax(A16, V + 1, 2048, 1, A16, A16, A16, 4, A16, None, A16, big, None) == -2
+    assert L.strata_head_argmax_margin(A16, V, 2048, 1, A16, A16, A16, 4, A16, A16, None, A16, big, None) == -2
+    assert L.strata_head_argmax_noalloc(A16, V, 2048, 1, A16, A16, A16, 4, A16, None, None) == -2
+
+
+def test_head_staged_activation_limit(L):
+    """Q8 with cols 16384 at T = 8: T*cols is at the staged maximum but the activation records and one
+    four-row slot do not fit shared memory; both head entry points say STRATA_ERR_SHAPE."""
+    ws = L.strata_head_argmax_workspace(1000, 8)
+    assert L.strata_head_argmax(A16, 1000, 16384, 1, A16, A16, A16, 8, A16, None, A16, ws, None) == -2
+    assert L.strata_head_argmax_noalloc(A16, 1000, 16384, 1, A16, A16, A16, 8, A16, None, None) == -2
+    assert L.strata_mmvq_multi(A16, 1000, 16384, 1, A16, A16, A16, 8, A16, None) == -2
+
+
+def test_wait_probe_rejects(L):
+    assert L.strata_wait_probe(0, -1, None) == -2
+    assert L.strata_wait_probe(2_000_000_000, -1, None) == -2
+    assert L.strata_wait_probe(1_000_000, 2_000_000_000, None) == -2
+
+
+def test_moe_gate_up_hook_rejects(L):
+    ws = L.strata_moe_grouped_workspace(128, 3256, 8, 2048, 768)
+    ok = [A16, 128, 2048, 768, A16, 3256, 8, A16, A16, A16, ws, None, A16, None]
+    a = list(ok); a[12] = None
+    assert L.strata_moe_grouped_gu(*a) == -1
+    a = list(ok); a[12] = A16 + 4
+    assert L.strata_moe_grouped_gu(*a) == -7
+    a = list(ok); a[10] = ws - 1
+    assert L.strata_moe_grouped_gu(*a) == -8
