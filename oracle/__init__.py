@@ -59,7 +59,8 @@ def _load():
             lib.or_margin.argtypes = [P, I64, I64, P]
             lib.or_moe_bucket.argtypes = [P, I64, I, I, P, P, P]
             lib.or_moe_bucket.restype = I64
-            lib.or_moe_rows.argtypes = [P, P, P, I, I64, I64, P, I64, I, P, P, I64, P, P, P, P, P, P, P, P]
+            lib.or_moe_rows.argtypes = [P, P, P, I, I64, I64, P, I64, I, P, P, I64, P, P, P, P, P, P, P, P,
+                                        P, P, P, P]
             lib.or_set_threads.argtypes = [I]
             lib.or_get_threads.restype = I
             _lib = lib
@@ -172,12 +173,14 @@ def moe_bucket(ids: np.ndarray, n_expert: int):
     return counts, offsets, pairs, int(bad)
 
 
-def moe_rows(experts, hidden, inter, ids, x, sel, want_hidden=False, hq_in=None, hd_in=None):
+def moe_rows(experts, hidden, inter, ids, x, sel, want_hidden=False, hq_in=None, hd_in=None,
+             want_gate_up=False):
     """MoE output rows for the pairs ``sel`` (p = tok*k + slot).
 
     ``experts``: list of (gate_buf, up_buf, down_buf) uint8 planar Q4 buffers.
     Returns dict with y, A (fp64 [n_sel][hidden]) and, with want_hidden, h (fp64 [n_sel][inter])
-    and its quantization hq/hd/hs. With hq_in/hd_in the down projection uses those rows.
+    and its quantization hq/hd/hs. With want_gate_up also g, u (fp64 [n_sel][inter]) and their
+    tolerance masses Ag, Au. With hq_in/hd_in the down projection uses those rows.
     """
     ids = _c(ids, np.int32)
     n_tok, k = ids.shape
@@ -197,12 +200,16 @@ def moe_rows(experts, hidden, inter, ids, x, sel, want_hidden=False, hq_in=None,
         hd = np.empty((n_sel, inter // 32), np.float32)
         hs = np.empty((n_sel, inter // 32), np.int32)
         out.update(h=h, hq=hq, hd=hd, hs=hs)
+    g = u = ag = au = None
+    if want_gate_up:
+        g, u, ag, au = (np.empty((n_sel, inter), np.float64) for _ in range(4))
+        out.update(g=g, u=u, Ag=ag, Au=au)
     hq_in = None if hq_in is None else _c(hq_in, np.int8)
     hd_in = None if hd_in is None else _c(hd_in, np.float32)
     _load().or_moe_rows(ctypes.cast(arr[0], ctypes.c_void_p), ctypes.cast(arr[1], ctypes.c_void_p),
                         ctypes.cast(arr[2], ctypes.c_void_p), n_expert, hidden, inter, _p(ids), n_tok, k,
                         _p(x), _p(sel), n_sel, _p(y), _p(A), _p(h), _p(hq), _p(hd), _p(hs),
-                        _p(hq_in), _p(hd_in))
+                        _p(hq_in), _p(hd_in), _p(g), _p(u), _p(ag), _p(au))
     return out
 
 

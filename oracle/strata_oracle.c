@@ -316,14 +316,16 @@ int64_t or_moe_bucket(const int32_t* ids, int64_t n_tok, int k, int n_expert,
 }
 
 /* The MoE output rows y[i][:] (fp64) and A[i][:] of the listed pairs sel[i] = tok*k + slot.
- * Optional (may be NULL): h[i][inter] fp64 hidden, hq/hd/hs its quantization.
+ * Optional (may be NULL): h[i][inter] fp64 hidden, hq/hd/hs its quantization; g[i][inter] and
+ * u[i][inter] the fp64 gate and up outputs with their tolerance masses ag, au (sum of |block terms|).
  * If hq_in/hd_in are given, the down projection takes THOSE quantized hidden rows (indexed by i)
  * instead of quantizing the oracle's own h. Pairs with an out-of-range id get y = NaN. */
 void or_moe_rows(const uint8_t* const* gate, const uint8_t* const* up, const uint8_t* const* down,
                  int n_expert, int64_t hidden, int64_t inter, const int32_t* ids, int64_t n_tok, int k,
                  const float* x, const int64_t* sel, int64_t n_sel, double* y, double* A,
                  double* h_out, int8_t* hq_out, float* hd_out, int32_t* hs_out,
-                 const int8_t* hq_in, const float* hd_in)
+                 const int8_t* hq_in, const float* hd_in,
+                 double* g_out, double* u_out, double* ag_out, double* au_out)
 {
     int64_t nbh = hidden / 32, nbi = inter / 32;
     (void)n_tok;
@@ -350,6 +352,8 @@ void or_moe_rows(const uint8_t* const* gate, const uint8_t* const* up, const uin
                 double g, ag, u, au;
                 row_dot(gate[e], inter, nbh, OR_Q4, c, xq, xd, &g, &ag);
                 row_dot(up[e], inter, nbh, OR_Q4, c, xq, xd, &u, &au);
+                if (g_out) { g_out[i * inter + c] = g; ag_out[i * inter + c] = ag; }
+                if (u_out) { u_out[i * inter + c] = u; au_out[i * inter + c] = au; }
                 h[c] = g / (1.0 + exp(-g)) * u;
                 hf[c] = (float)h[c];
             }

@@ -1,10 +1,12 @@
 """GPU parity of the prompt-chunk MoE (strata_moe_grouped) against the CPU oracle.
 
-Bars: the per-expert grouping equals the oracle's exactly; the down projection's integer dots are
-pinned by feeding the GPU's own re-quantized hidden rows to the oracle (so y must then lie within
-the fp32 bound); the re-quantized hidden codes equal the oracle's up to a one-step flip where fp32
-SiLU rounding moves a value across a rounding boundary; out-of-range ids set the error word and
-leave their rows untouched.
+Bars: the per-expert grouping equals the oracle's exactly; the fp32 gate and up outputs g, u (read
+back through the strata_moe_grouped_gu test hook, which runs the same kernels) lie element by element
+within the stated bound |gpu - oracle| <= 2e-6 * sum|block terms| + 1e-6 of the oracle's fp64 g, u;
+the down projection's integer dots are pinned by feeding the GPU's own re-quantized hidden rows to
+the oracle (so y must then lie within the fp32 bound); the re-quantized hidden codes equal the
+oracle's up to a one-step flip where fp32 SiLU rounding moves a value across a rounding boundary;
+out-of-range ids set the error word and leave their rows untouched.
 """
 import numpy as np
 import pytest
@@ -42,15 +44,16 @@ class MoeCase:
     def bufs(self):
         return [(g.buf, u.buf, d.buf) for g, u, d in self.host]
 
-    def run(self, ids=None, y_init=None):
+    def run(self, ids=None, y_init=None, with_gu=True):
         ids = self.ids if ids is None else ids
         ws = torch.empty(strata.moe_grouped_workspace(self.n_exp, self.n_tok, self.k, self.hidden, self.inter),
                          dtype=torch.uint8, device="cuda")
         err = torch.full((1,), -7, dtype=torch.int32, device="cuda")
         y = (torch.full((self.n_tok * self.k, self.hidden), float(y_init), device="cuda")
              if y_init is not None else None)
+        gu = (torch.full((self.n_tok * self.k, 2, self.inter), float("nan"), device="cuda") if with_gu else None)
         y = strata.moe_grouped(self.tab, self.n_exp, self.hidden, self.inter, cu(ids), cu(self.x), y=y,
-                               workspace=ws, err_word=err)
+                               workspace=ws, err_word=err, gu=gu)
         torch.cuda.synchronize()
         v = strata.moe_debug_views(self.n_exp, self.n_tok, self.k, self.hidden, self.inter)
         wsn = ws.cpu().numpy()
@@ -64,6 +67,7 @@ class MoeCase:
             hq=wsn[v["hq"]:v["hq"] + n_pair * self.inter].view(np.int8).reshape(n_pair, self.inter).copy(),
             hd=wsn[v["hd"]:v["hd"] + 4 * n_pair * nbi].view(np.float32).reshape(n_pair, nbi).copy(),
             hs=wsn[v["hs"]:v["hs"] + 4 * n_pair * nbi].view(np.int32).reshape(n_pair, nbi).copy())
+        out["gu"] = gu.cpu().numpy() if with_gu else None
         return out
 
 
@@ -75,7 +79,14 @@ def check_rows(case, out, sel):
     pos_of[out["pairs"][:n_valid]] = np.arange(n_valid)
     pos = pos_of[sel]
     ref = oracle.moe_rows(case.bufs(), case.hidden, case.inter, case.ids, case.x, sel, want_hidden=True,
-                          hq_in=out["hq"][pos], hd_in=out["hd"][pos])
+                          hq_in=out["hq"][pos], hd_in=out["hd"][pos], want_gate_up=out["gu"] is not None)
+    if out["gu"] is not None:
+        # gate and up at the stated bound, element by element
+        for plane, name, mass in ((0, "g", "Ag"), (1, "u", "Au")):
+            got = out["gu"][sel, plane].astype(np.float64)
+            e = np.abs(got - ref[name])
+            t = oracle.tolerance(ref[mass])
+            assert (e <= t).all(), f"{name}: {(e > t).sum()} of {e.size} outside the bound, worst {(e / t).max():.3g}x"
     tol = oracle.tolerance(ref["A"])
     err = np.abs(out["y"][sel].astype(np.float64) - ref["y"])
     assert (err <= tol).all(), f"{(err > tol).sum()} of {err.size} y values outside the bound"
@@ -118,6 +129,7 @@ def test_moe_bad_ids_flag_and_skip():
     assert out["err"] == 1
     bad = [3 * 2 + 1, 17 * 2 + 0, 39 * 2 + 1]
     assert (out["y"][bad] == 123.0).all()
+    assert np.isnan(out["gu"][bad]).all()                     # the hook skips them too
     counts, offsets, pairs, nbad = oracle.moe_bucket(ids, 8)
     assert nbad == 3 and np.array_equal(out["pairs"][:offsets[-1]], pairs[:offsets[-1]])
     good = np.setdiff1d(np.arange(80), bad)
@@ -144,10 +156,12 @@ def test_moe_prompt_chunk_sampled(c5):
     sample = rng.choice(c5.n_tok * c5.k, size=(c5.n_tok * c5.k) * 3 // 100, replace=False)
     sel = np.unique(np.concatenate([heavy, light, sample]))
     check_rows(c5, out, sel)
-    # every row written exactly once: a second run with a NaN-filled y leaves no NaN
-    out2 = c5.run(y_init=float("nan"))
+    # every row written exactly once: a second run, through the product entry point, with a NaN-filled
+    # y leaves no NaN and equals the test hook's run bit for bit (same kernels)
+    out2 = c5.run(y_init=float("nan"), with_gu=False)
     assert not np.isnan(out2["y"]).any()
     assert np.array_equal(out2["y"], out["y"])
+    assert not np.isnan(out["gu"]).any()
 
 
 def test_moe_idle_experts_get_no_tiles():

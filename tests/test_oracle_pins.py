@@ -237,7 +237,7 @@ def test_moe_rows_brute_force(orc):
     x = synth.make_activations(n_tok, hidden, "moe-bf")
     sel = np.arange(n_tok * k)
     out = orc.moe_rows([(g.buf, u.buf, d.buf) for g, u, d in experts], hidden, inter, ids, x, sel,
-                       want_hidden=True)
+                       want_hidden=True, want_gate_up=True)
     xq, xd, _ = orc.quantize_act(x)
     xdeq = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
     for p in sel:
@@ -246,6 +246,14 @@ def test_moe_rows_brute_force(orc):
         u = dense_dequant(experts[e][1]) @ xdeq[tok]
         h = g * u / (1.0 + np.exp(-g))
         assert np.allclose(out["h"][p], h, rtol=1e-12, atol=1e-300)
+        # the gate and up outputs and their masses: the dense values, and A = sum |d_w d_x isum| per
+        # block written out here from the unpacked codes and scales
+        for name, mass, ref, wm in (("g", "Ag", g, experts[e][0]), ("u", "Au", u, experts[e][1])):
+            assert np.all(np.abs(out[name][p] - ref) <= 1e-12 * out[mass][p] + 1e-300)
+            qq = wm.codes().astype(np.int64).reshape(inter, hidden // 32, 32) - 8
+            isum = np.einsum("rbj,bj->rb", qq, xq[tok].astype(np.int64).reshape(hidden // 32, 32))
+            terms = wm.scales.astype(np.float64) * xd[tok].astype(np.float64)[None, :] * isum
+            assert np.allclose(out[mass][p], np.abs(terms).sum(axis=1), rtol=1e-12, atol=0)
         hdeq = out["hq"][p].astype(np.float64) * np.repeat(out["hd"][p].astype(np.float64), 32)
         yref = dense_dequant(experts[e][2]) @ hdeq
         assert np.all(np.abs(out["y"][p] - yref) <= 1e-12 * out["A"][p] + 1e-300)
@@ -515,18 +523,28 @@ def test_quantizer_is_blockwise_so_inputs_concatenate(orc):
     assert np.array_equal(sf[0], np.concatenate(ss))
 
 
-@pytest.mark.parametrize("fmt", [2, 3, 4])
-def test_superblock_tolerance_mass_is_sum_of_abs_terms(orc, fmt):
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+def test_tolerance_mass_is_sum_of_abs_terms(orc, fmt):
     """A (the tolerance's mass) is the sum of |term| over the format's terms, computed here from the
-    unpacked fields: Q6 one term per 16 weights (d*s*d_x*isum16), Q4K / Q5K two per block
-    (d*sc*d_x*isum and -dmin*m*d_x*sum x). A too-large A would loosen every GPU comparison."""
+    unpacked fields: Q4 / Q8 one term per block (d_w*d_x*isum, isum = sum (q-8)x or sum qx), Q6 one
+    per 16 weights (d*s*d_x*isum16), Q4K / Q5K two per block (d*sc*d_x*isum and -dmin*m*d_x*sum x).
+    A too-large A (say summed twice, or summed over the signed terms' absolute total) would loosen
+    every GPU comparison; rows hold many blocks with terms of both signs, so such a mistake shows."""
     rng = np.random.default_rng(53 + fmt)
     rows, cols, T = 3, 512, 2
     nb = cols // 32
     xq, xd, _ = orc.quantize_act(rng.standard_normal((T, cols)).astype(np.float32))
     x = xq.astype(np.int64).reshape(T, nb, 32)
     dx = xd.astype(np.float64)
-    if fmt == 2:
+    if fmt in (0, 1):
+        q = (rng.integers(0, 16, size=(rows, cols)) if fmt == 0 else rng.integers(-127, 128, size=(rows, cols)))
+        d = (np.abs(rng.standard_normal((rows, nb))) * 0.01).astype(np.float16)
+        W = pack_q4(q, d) if fmt == 0 else pack_q8(q, d)
+        qq = q.astype(np.int64).reshape(rows, nb, 32) - (8 if fmt == 0 else 0)
+        isum = np.einsum("rbj,tbj->trb", qq, x)
+        terms = d.astype(np.float64)[None] * dx[:, None, :] * isum
+        assert (terms > 0).any() and (terms < 0).any()
+    elif fmt == 2:
         q = rng.integers(0, 64, size=(rows, cols)).astype(np.uint8)
         sub = rng.integers(-127, 128, size=(rows, cols // 16)).astype(np.int8)
         d = (np.abs(rng.standard_normal((rows, cols // 256))) * 0.001).astype(np.float16)
