@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-configs", action="store_true", help="skip the decode GEMV and verify FFN lines")
     ap.add_argument("--case", default="window",
                     choices=["window", "mmvq", "head", "moe", "layers", "mma_peaks", "gemm"],
                     help="window: the timed step; mmvq/head/moe/layers: a few launches of one kernel "
@@ -86,58 +86,49 @@ def peaks():
         return 6800.0, "fallback"
 
 
-# ---- CPU oracle baseline (bounded sample of the same workload) -------------------------------------
-class OracleSample:
-    """The oracle on a bounded sample of the window: the first layers' matrices and the head, each
-    over its first ``frac`` of rows, at T tokens. ``rate()`` scales the sample's time by its share
-    of the window's weight-times-token work to give the oracle's window tokens/s on this host."""
+# ---- CPU oracle baseline: the whole window ----------------------------------------------------------
+class OracleWindow:
+    """The oracle on the full verify window as it stands: each projection's T input rows quantized,
+    every row of every layer matrix and of the head at T tokens, the head's argmax. ``run()`` is one
+    whole window; ``run(n_layer_mats)`` covers only the first layer matrices and the head (a bounded
+    sample for long reference runs) and returns the share of the window's weight x token work it did.
+    The oracle runs one OpenMP thread per core this process may use (sched_getaffinity)."""
 
     def __init__(self, T: int, layers: int, host_weights=None):
         import oracle
         from block_quantized_token_strata_gb300 import synth
         oracle.build()
+        self.cores = len(os.sched_getaffinity(0))
+        oracle.set_threads(self.cores)
         self.oracle, self.T = oracle, T
         shapes = synth.window_shapes(layers)
-        idx = list(range(min(8, 4 * layers))) + [len(shapes) - 1]
         self.total = sum(r * c for _, r, c, _ in shapes)
         self.mats = []
-        for i in idx:
-            name, rows, cols, fmt = shapes[i]
+        for i, (name, rows, cols, fmt) in enumerate(shapes):
             w = host_weights[i] if host_weights is not None else synth.make_weights(rows, cols, fmt, "window", name)
-            x = synth.make_activations(T, cols, "window-x", name)
-            self.mats.append((name, w, rows, cols, fmt, x))
+            self.mats.append((name, w.buf, rows, cols, fmt, synth.make_activations(T, cols, "window-x", name)))
 
-    def run(self, frac: float) -> float:
-        """One pass over the sample; returns the fraction of the window's work it covered."""
-        o, part = self.oracle, 0
-        for name, w, rows, cols, fmt, x in self.mats:
-            n = max(1, int(rows * frac))
+    def run(self, n_layer_mats: int | None = None) -> float:
+        o = self.oracle
+        sel = self.mats if n_layer_mats is None else self.mats[:n_layer_mats] + self.mats[-1:]
+        part = 0
+        for name, buf, rows, cols, fmt, x in sel:
             xq, xd, _ = o.quantize_act(x)
-            y, _ = o.mmvq_rows(w.buf, rows, cols, fmt, xq, xd, np.arange(n))
+            y, _ = o.mmvq(buf, rows, cols, fmt, xq, xd)
             if name == "head":
                 o.argmax(y)
-            part += n * cols
+            part += rows * cols
         return part / self.total
 
-    def calibrate(self, seconds: float) -> float:
-        t0 = time.perf_counter()
-        share = self.run(0.01)
-        el = max(time.perf_counter() - t0, 1e-4)
-        return float(min(1.0, max(0.001, 0.01 * seconds / el)))
-
-    def rate(self, seconds: float):
-        frac = self.calibrate(min(seconds, 5.0))
-        reps, t0 = 0, time.perf_counter()
-        while True:
-            share = self.run(frac)
-            reps += 1
-            el = time.perf_counter() - t0
-            if el >= seconds:
-                break
-        per_window = el / reps / share
-        desc = (f"first {frac:.2%} of the rows of {len(self.mats) - 1} layer matrices and of the head "
-                f"({share:.2%} of the window's weight x token work per pass), T={self.T}, {reps} passes")
-        return self.T / per_window, self.oracle.get_threads(), desc
+    def full_rate(self, reps: int = 3):
+        """Median wall time of ``reps`` whole windows -> (tokens/s, seconds per window)."""
+        times = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            self.run()
+            times.append(time.perf_counter() - t0)
+        per = statistics.median(times)
+        return self.T / per, per
 
 
 # ---- clocks ----------------------------------------------------------------------------------------
@@ -184,30 +175,40 @@ class ClockSampler:
 
 # ---- reference arm -------------------------------------------------------------------------------------
 def run_reference(args, rank: int) -> None:
-    """The CPU oracle timed as it stands, each step a bounded sample sized so that the whole
-    --steps/--warmup run takes about two minutes."""
+    """The CPU oracle timed as it stands on the same window. Each step is one whole window when the
+    --steps/--warmup run fits in about four minutes that way (the normal case); for longer runs each
+    step covers the first layer matrices and the head, and the line says so."""
     if rank != 0:
         return
-    smp = OracleSample(args.T, args.layers)
-    per_step = max(0.05, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
-    frac = smp.calibrate(per_step)
-    for _ in range(args.warmup):
-        smp.run(frac)
-    times, share = [], None
+    smp = OracleWindow(args.T, args.layers)
+    t0 = time.perf_counter()
+    smp.run()                                   # the first warm-up step, timed to size the rest
+    t_full = time.perf_counter() - t0
+    n_steps = args.steps + max(args.warmup - 1, 0)
+    n_mats = None
+    if n_steps * t_full > 240.0:                # bounded sample per step
+        share_target = max(0.01, 240.0 / n_steps / t_full)
+        n_mats = max(1, int(share_target * (len(smp.mats) - 1)))
+    for _ in range(max(args.warmup - 1, 0)):
+        smp.run(n_mats)
+    times, share = [], 1.0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        share = smp.run(frac)
+        share = smp.run(n_mats)
         times.append(time.perf_counter() - t0)
     per_window = statistics.median(times) / share
     value = args.T / per_window
-    sample = (f"per step: first {frac:.2%} of the rows of 8 layer matrices and of the head "
-              f"({share:.2%} of the window's weight x token work), T={args.T}; time scaled to a full window")
+    if n_mats is None:
+        sample = f"per step one whole window (192 layer matrices + the head, T={args.T}); median of {args.steps} steps"
+    else:
+        sample = (f"per step the first {n_mats} layer matrices and the head ({share:.2%} of the window's weight x "
+                  f"token work), T={args.T}; time divided by that share")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_window,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "T": args.T, "layers": args.layers},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.oracle.get_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -418,10 +419,17 @@ def main():
         q6 = {name: bench_superblock_layers(torch, strata, synth, hbm_peak, fmt)
               for name, fmt in (("Q6", synth.Q6), ("Q4K", synth.Q4K), ("Q5K", synth.Q5K))}
 
+    decode = ffn = None
+    if not args.no_configs:
+        decode = bench_decode(torch, strata, synth, hbm_peak)
+        ffn = bench_verify_ffn(torch, strata, synth, hbm_peak)
+
     cpu = None
     if rank == 0 and not args.no_cpu:
-        rate, cores, sample = OracleSample(T, args.layers, wts.host).rate(args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+        ow = OracleWindow(T, args.layers, wts.host)
+        rate, per = ow.full_rate(3)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": ow.cores, "kind": "oracle",
+               "sample": f"3 whole windows (192 layer matrices + the head, T={T}), median {per:.2f} s a window"}
 
     if rank == 0:
         line = {
@@ -439,12 +447,130 @@ def main():
             "per_T": per_T, "chained_launches": chained, "batch_head_margin": hb, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "moe": moe, "prompt_gemm": gemm,
-            "superblock_layers": q6,
+            "superblock_layers": q6, "decode_gemv": decode, "verify_ffn": ffn,
             "device_error_word": strata.device_error(),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _graph(torch, fn):
+    """One CUDA graph of fn() (after one eager pass on a side stream)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _time_graph(torch, g, reps):
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _rotating_copies(torch, nbytes):
+    """How many weight copies make ceil(3 L2 / size): a rotation through them streams from HBM."""
+    l2 = int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    return max(2, -(-3 * l2 // nbytes)), l2
+
+
+def bench_decode(torch, strata, synth, hbm_peak, reps=20):
+    """Decode GEMV: one token (T = 1) through a 4096 x 4096 matrix in Q4 and in Q8, activations N(0,1)
+    with 1% of elements x20, one quantize launch + one GEMV launch a step. The matrix fits in L2, so
+    the steps run as one CUDA graph over ceil(3 L2 / size) weight copies in turn (each step reads
+    its copy from HBM)."""
+    rows = cols = 4096
+    x = torch.from_numpy(synth.make_activations(1, cols, "decode", outliers=True)).cuda()
+    xq = torch.empty((1, cols), dtype=torch.int8, device="cuda")
+    xd = torch.empty((1, cols // 32), dtype=torch.float32, device="cuda")
+    xs = torch.empty((1, cols // 32), dtype=torch.int32, device="cuda")
+    y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+    out = {"workload": "4096x4096, T=1, activations with 1% outliers x20; quantize + GEMV per step"}
+    for name, fmt in (("Q4", synth.Q4), ("Q8", synth.Q8)):
+        nbytes = synth.weight_nbytes(rows, cols, fmt)
+        n, l2 = _rotating_copies(torch, nbytes)
+        W0 = torch.from_numpy(synth.make_weights(rows, cols, fmt, "decode").buf).cuda()
+        copies = [W0.clone() for _ in range(n)]
+
+        def steps():
+            for Wc in copies:
+                strata.quantize_act(x, xq, xd, xs)
+                strata.mmvq_multi(Wc, rows, cols, fmt, xq, xd, xs, 1, y)
+        g = _graph(torch, steps)
+        ms = _time_graph(torch, g, reps) / n
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": ms * 1e3, "tokens_per_s": 1.0 / (ms * 1e-3), "weight_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+                     "roofline_us": nbytes / (hbm_peak * 1e9) * 1e6, "weight_bytes": nbytes, "copies": n,
+                     "l2_bytes": l2}
+        del g, copies, W0
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_verify_ffn(torch, strata, synth, hbm_peak, reps=20):
+    """Verify-window FFN: a Q4 up projection 4096 -> 14336 and a down projection 14336 -> 4096 (66 MB)
+    at T = 1/2/3/4/8 columns, each input its own seeded N(0,1) rows (no activation function between
+    them). Per step either one quantize launch over both inputs + one grouped GEMV launch of the two
+    matrices ("grouped"), or a quantize + GEMV launch per projection ("chained"). Timed as one CUDA
+    graph over ceil(3 L2 / size) weight copies in turn."""
+    H, F = 4096, 14336
+    shapes = (("up", F, H), ("down", H, F))
+    nbytes = sum(synth.weight_nbytes(r, c, synth.Q4) for _, r, c in shapes)
+    n, l2 = _rotating_copies(torch, nbytes)
+    base = [torch.from_numpy(synth.make_weights(r, c, synth.Q4, "verify-ffn", nm).buf).cuda() for nm, r, c in shapes]
+    copies = [[b.clone() for b in base] for _ in range(n)]
+    out = {"workload": "Q4 up 4096->14336 + down 14336->4096, independent inputs", "weight_bytes": nbytes,
+           "copies": n, "roofline_us": nbytes / (hbm_peak * 1e9) * 1e6}
+    for T in (1, 2, 3, 4, 8):
+        tot = T * (H + F)
+        xf = torch.from_numpy(np.concatenate([synth.make_activations(T, c, "verify-ffn-x", nm).reshape(-1)
+                                              for nm, _, c in shapes])).cuda()
+        qf = torch.empty(tot, dtype=torch.int8, device="cuda")
+        df = torch.empty(tot // 32, dtype=torch.float32, device="cuda")
+        sf = torch.empty(tot // 32, dtype=torch.int32, device="cuda")
+        xs_ = [xf[:T * H].view(T, H), xf[T * H:].view(T, F)]
+        qs = [qf[:T * H].view(T, H), qf[T * H:].view(T, F)]
+        ds = [df[:T * H // 32].view(T, H // 32), df[T * H // 32:].view(T, F // 32)]
+        ss = [sf[:T * H // 32].view(T, H // 32), sf[T * H // 32:].view(T, F // 32)]
+        ys = [torch.empty((T, r), dtype=torch.float32, device="cuda") for _, r, _ in shapes]
+        descs = [strata.gemv_descs([(cp[i], shapes[i][1], shapes[i][2], qs[i], ds[i], ss[i], ys[i]) for i in range(2)])
+                 for cp in copies]
+
+        def grouped():
+            for d in descs:
+                strata.quantize_act(xf.view(1, -1), qf.view(1, -1), df.view(1, -1), sf.view(1, -1))
+                strata.mmvq_grouped(d, synth.Q4, T)
+
+        def chained():
+            for cp in copies:
+                for i, (_, r, c) in enumerate(shapes):
+                    strata.quantize_act(xs_[i], qs[i], ds[i], ss[i])
+                    strata.mmvq_multi(cp[i], r, c, synth.Q4, qs[i], ds[i], ss[i], T, ys[i])
+        line = {}
+        for mode, fn in (("grouped", grouped), ("chained", chained)):
+            g = _graph(torch, fn)
+            ms = _time_graph(torch, g, reps) / n
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            line[mode] = {"us": ms * 1e3, "tokens_per_s": T / (ms * 1e-3), "weight_gbs": gbs,
+                          "hbm_frac": gbs / hbm_peak}
+            del g
+        out[f"T{T}"] = line
+    del copies, base
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_superblock_layers(torch, strata, synth, hbm_peak, fmt, layers=16, reps=20):
