@@ -264,8 +264,9 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     float* hv = red + 2 * kCW * 32;                                      // head: [kCW*32] values
     int* hi = reinterpret_cast<int*>(hv + kCW * 32);                     // head: [kCW*32] ids
     float* hs = reinterpret_cast<float*>(hi + kCW * 32);                 // head: [kCW*32] second values
-    uint8_t* cring = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(hs + kCW * 32) + 127) & ~uintptr_t(127));   // codes [NST][cstage]
+    // codes [NST][cstage]: an offset from `smem` (not an integer round trip), so that the compiler keeps
+    // the ring in the shared address space and its reads stay shared-memory loads
+    uint8_t* cring = smem + ((reinterpret_cast<uint8_t*>(hs + kCW * 32) - smem + 127) & ~ptrdiff_t(127));
     uint8_t* sring = cring + NST * p.cstage;                                      // scales [NST][sstage]
     uint8_t* dring = sring + NST * p.sstage;                                      // Q6 d [NST][dstage]
 
