@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libstrata.so")
-SOURCES = ["abi.cu", "quantize.cu", "mmvq.cu", "moe.cu", "head_noalloc.cu", "wait_probe.cu"]
+SOURCES = ["abi.cu", "quantize.cu", "mmvq.cu", "moe.cu", "gemm_dequant.cu", "head_noalloc.cu", "wait_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -14,6 +14,25 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? STRATA_OK : STRATA_ERR_CUDA; }
 
+}  // namespace
+
+namespace strata {
+// the device error word as the C ABI reports it: the copies of every translation unit whose kernels
+// set it, ORed
+cudaError_t read_device_error(int* out, bool clear)
+{
+    int a = 0, b = 0, c = 0, d = 0;
+    cudaError_t e = read_device_error_gemv(&a, clear);
+    if (e == cudaSuccess) e = read_device_error_moe(&b, clear);
+    if (e == cudaSuccess) e = read_device_error_probe(&c, clear);
+    if (e == cudaSuccess) e = read_device_error_gemm(&d, clear);
+    *out = a | b | c | d;
+    return e;
+}
+}  // namespace strata
+
+namespace {
+
 int check_matrix(int64_t rows, int64_t cols, int fmt)
 {
     if (fmt != STRATA_Q4 && fmt != STRATA_Q8 && fmt != STRATA_Q6 && fmt != STRATA_Q4K && fmt != STRATA_Q5K)
@@ -162,6 +181,25 @@ int strata_gemm_q4(const void* W, int64_t rows, int64_t cols, const int8_t* xq, 
     if (rows > 65536 || cols > 65536 || n_tok > (int64_t(1) << 24)) return STRATA_ERR_SHAPE;
     if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(xd, 4) || !aligned(y, 16)) return STRATA_ERR_ALIGN;
     return cuda_status(launch_prompt_gemm(W, rows, cols, xq, xd, n_tok, y, stream));
+}
+
+size_t strata_gemm_q4_dequant_workspace(int64_t rows, int64_t cols, int64_t n_tok)
+{
+    if (rows < 128 || rows % 128 != 0 || cols < 64 || cols % 64 != 0 || n_tok < 1) return 0;
+    if (rows > 65536 || cols > 65536 || n_tok > (int64_t(1) << 24)) return 0;
+    return gemm_dequant_workspace_bytes(rows, cols, n_tok);
+}
+
+int strata_gemm_q4_dequant(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                           int64_t n_tok, float* y, void* workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!W || !xq || !xd || !y) return STRATA_ERR_NULL;
+    if (rows < 128 || rows % 128 != 0 || cols < 64 || cols % 64 != 0 || n_tok < 1) return STRATA_ERR_SHAPE;
+    if (rows > 65536 || cols > 65536 || n_tok > (int64_t(1) << 24)) return STRATA_ERR_SHAPE;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(xd, 4) || !aligned(y, 16)) return STRATA_ERR_ALIGN;
+    if (!workspace || ws_bytes < gemm_dequant_workspace_bytes(rows, cols, n_tok)) return STRATA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return STRATA_ERR_ALIGN;
+    return cuda_status(launch_gemm_dequant(W, rows, cols, xq, xd, n_tok, y, workspace, stream));
 }
 
 int strata_block_dots(const void* W, int64_t rows, int64_t cols, int fmt, const int8_t* xq, const int32_t* xs,

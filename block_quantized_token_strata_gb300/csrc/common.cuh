@@ -102,7 +102,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
 // this header holds its own copy; each unit whose kernels set it exports a host reader (internal.h)
 // and strata_device_error combines them.
 static __device__ int g_strata_device_error = 0;
-// generic-proxy shared-memory writes before later async-proxy (TMA) accesses of the same bytes
+// orders this thread's generic-proxy shared-memory accesses (writes, and reads of a slot about to
+// be refilled) before later async-proxy (bulk copy, TMA, tensor core) accesses of the same bytes
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -55,6 +55,7 @@ cudaError_t read_device_error(int* out, bool clear);
 cudaError_t read_device_error_gemv(int* out, bool clear);
 cudaError_t read_device_error_moe(int* out, bool clear);
 cudaError_t read_device_error_probe(int* out, bool clear);
+cudaError_t read_device_error_gemm(int* out, bool clear);
 // test hook: one CTA waits, bounded by limit_ns, on an mbarrier nobody arrives at (abort_after_ns
 // >= 0: a second warp raises the CTA's abort flag after that long instead)
 cudaError_t launch_wait_probe(int64_t limit_ns, int64_t abort_after_ns, cudaStream_t stream);
@@ -86,5 +87,9 @@ cudaError_t launch_moe_grouped(const void* experts, int n_expert, int64_t hidden
                                cudaStream_t stream);
 cudaError_t launch_prompt_gemm(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
                                int64_t n_tok, float* y, cudaStream_t stream);
+// the prompt GEMM's wide-dequant arm (gemm_dequant.cu)
+size_t gemm_dequant_workspace_bytes(int64_t rows, int64_t cols, int64_t n_tok);
+cudaError_t launch_gemm_dequant(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                                int64_t n_tok, float* y, void* workspace, cudaStream_t stream);
 
 }  // namespace strata

@@ -1160,15 +1160,5 @@ cudaError_t read_device_error_gemv(int* out, bool clear)
     return cudaMemcpyToSymbol(g_strata_device_error, &zero, sizeof(int));
 }
 
-// the word as the C ABI reports it: the copies of every translation unit whose kernels set it, ORed
-cudaError_t read_device_error(int* out, bool clear)
-{
-    int a = 0, b = 0, c = 0;
-    cudaError_t e = read_device_error_gemv(&a, clear);
-    if (e == cudaSuccess) e = read_device_error_moe(&b, clear);
-    if (e == cudaSuccess) e = read_device_error_probe(&c, clear);
-    *out = a | b | c;
-    return e;
-}
 
 }  // namespace strata

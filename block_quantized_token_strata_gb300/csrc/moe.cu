@@ -456,9 +456,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const MoeTcArgs a
                 for (int half = 0; half < 2; ++half) {
                     const int c0 = PHASE == 0 ? 32 * cg + 64 * half : 64 * cg + 32 * half;  // tile column
                     uint32_t v[2][16];  // both 16-column loads of the half in flight, one wait
-                    tmem_ld16(tl + buf * 128 + c0, v[0]);
-                    tmem_ld16(tl + buf * 128 + c0 + 16, v[1]);
-                    tmem_ld_wait();
+                    tmem_ld32(tl + buf * 128 + c0, v);
 #pragma unroll
                     for (int q16 = 0; q16 < 2; ++q16) {
                         const float4* dw4 = reinterpret_cast<const float4*>(sl + 128 + c0 + 16 * q16);

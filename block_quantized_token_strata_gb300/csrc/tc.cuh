@@ -65,7 +65,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
                    "=r"(v[14]), "=r"(v[15])
                  : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The registers a tcgen05.ld writes are valid only after tcgen05.wait::ld, yet the compiler sees them
+// as defined by the load itself and may schedule arithmetic that reads them ahead of a wait that names
+// no registers. So the wait takes the loaded registers as read-write operands: every use stays below
+// it. Two 16-column loads go out back to back and one wait covers both.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[2][16]) {
+    tmem_ld16(taddr, v[0]);
+    tmem_ld16(taddr + 16, v[1]);
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0][0]),"+r"(v[0][1]),"+r"(v[0][2]),"+r"(v[0][3]),"+r"(v[0][4]),"+r"(v[0][5]),"+r"(v[0][6]),"+r"(v[0][7]),
+                   "+r"(v[0][8]),"+r"(v[0][9]),"+r"(v[0][10]),"+r"(v[0][11]),"+r"(v[0][12]),"+r"(v[0][13]),"+r"(v[0][14]),"+r"(v[0][15]),
+                   "+r"(v[1][0]),"+r"(v[1][1]),"+r"(v[1][2]),"+r"(v[1][3]),"+r"(v[1][4]),"+r"(v[1][5]),"+r"(v[1][6]),"+r"(v[1][7]),
+                   "+r"(v[1][8]),"+r"(v[1][9]),"+r"(v[1][10]),"+r"(v[1][11]),"+r"(v[1][12]),"+r"(v[1][13]),"+r"(v[1][14]),"+r"(v[1][15])
+                 :: "memory");
+}
 
 // ---- exact small integers as fp16 pairs ----------------------------------------------------------
 // Bytes b0, b1 of `bytes` (selected by `sel`) become the fp16 pair (1024 + b0, 1024 + b1): the

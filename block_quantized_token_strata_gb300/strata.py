@@ -66,11 +66,14 @@ def lib() -> ctypes.CDLL:
             L.strata_gemm_q4.argtypes = [P, I64, I64, P, P, I64, P, P]
             L.strata_moe_grouped_gu.argtypes = [P, I, I64, I64, P, I64, I, P, P, P, SZ, P, P, P]
             L.strata_wait_probe.argtypes = [I64, I64, P]
+            L.strata_gemm_q4_dequant_workspace.argtypes = [I64, I64, I64]
+            L.strata_gemm_q4_dequant_workspace.restype = SZ
+            L.strata_gemm_q4_dequant.argtypes = [P, I64, I64, P, P, I64, P, P, SZ, P]
             for name in ("strata_quantize_act", "strata_mmvq_multi", "strata_head_argmax",
                          "strata_moe_grouped", "strata_moe_debug_views", "strata_block_dots",
                          "strata_mmvq_grouped", "strata_device_error", "strata_head_argmax_noalloc",
                          "strata_head_argmax_margin", "strata_gemm_q4", "strata_moe_grouped_gu",
-                         "strata_wait_probe"):
+                         "strata_wait_probe", "strata_gemm_q4_dequant"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -199,6 +202,24 @@ def gemm_q4(W, rows: int, cols: int, xq, xd, y=None, stream=None):
         y = torch.empty((n_tok, rows), dtype=torch.float32, device=xq.device)
     _check(lib().strata_gemm_q4(_ptr(W), rows, cols, _ptr(xq), _ptr(xd), n_tok, _ptr(y), _stream(stream)),
            "strata_gemm_q4")
+    return y
+
+
+def gemm_q4_dequant_workspace(rows: int, cols: int, n_tok: int) -> int:
+    return int(lib().strata_gemm_q4_dequant_workspace(rows, cols, n_tok))
+
+
+def gemm_q4_dequant(W, rows: int, cols: int, xq, xd, y=None, workspace=None, stream=None):
+    """The dense prompt GEMM's wide-dequant arm: same result as gemm_q4, bit for bit."""
+    n_tok = xq.shape[0]
+    if y is None:
+        y = torch.empty((n_tok, rows), dtype=torch.float32, device=xq.device)
+    need = gemm_q4_dequant_workspace(rows, cols, n_tok)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else need
+    _check(lib().strata_gemm_q4_dequant(_ptr(W), rows, cols, _ptr(xq), _ptr(xd), n_tok, _ptr(y), _ptr(workspace),
+                                        ws_bytes, _stream(stream)), "strata_gemm_q4_dequant")
     return y
 
 

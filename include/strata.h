@@ -263,6 +263,22 @@ int strata_gemm_q4(const void* W, int64_t rows, int64_t cols, const int8_t* xq, 
                    int64_t n_tok, float* y, cudaStream_t stream);
 
 /*
+ * strata_gemm_q4_dequant — the same dense prompt-chunk GEMM in the "wide dequant" arm of the Strata
+ * pull request "sm_80 (GA100) tuning" (commit message on STRATA_DEQUANT_WIDE: the dense weights are
+ * dequantized once per prompt chunk, then multiplied). A conversion pass writes the weight codes
+ * q - 8 and the activation codes as fp16 (exact) into the workspace, in 128 x 32 tiles already in the
+ * tensor cores' shared-memory order, with the matching d_w and d_x vectors; the GEMM then streams
+ * them with bulk copies. Same arguments, rules and results as strata_gemm_q4, bit for bit (the same
+ * block arithmetic in the same order), plus:
+ *   workspace : strata_gemm_q4_dequant_workspace(rows, cols, n_tok) bytes, device, 256-byte aligned;
+ *               contents need no initialisation and are dead after the call.
+ *   Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA; a timed-out wait sets bit 0 of the device error word.
+ */
+size_t strata_gemm_q4_dequant_workspace(int64_t rows, int64_t cols, int64_t n_tok);
+int strata_gemm_q4_dequant(const void* W, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                           int64_t n_tok, float* y, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * strata_moe_grouped — prompt-chunk MoE experts: per (token, slot) pair p = tok*k + slot routed to
  * expert e = ids[p]:
  *     g = W_gate[e] . xq(tok), u = W_up[e] . xq(tok)         (block arithmetic above, fp32)

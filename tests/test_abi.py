@@ -175,3 +175,18 @@ def test_moe_gate_up_hook_rejects(L):
     assert L.strata_moe_grouped_gu(*a) == -7
     a = list(ok); a[10] = ws - 1
     assert L.strata_moe_grouped_gu(*a) == -8
+
+
+def test_gemm_dequant_rejects(L):
+    ws = L.strata_gemm_q4_dequant_workspace(6144, 2048, 3259)
+    assert ws >= 48 * 64 * 8192 + 26 * 64 * 8192
+    assert L.strata_gemm_q4_dequant_workspace(200, 2048, 10) == 0
+    ok = [A16, 256, 512, A16, A16, 300, A16, A16, 1 << 30, None]
+    a = list(ok); a[0] = None
+    assert L.strata_gemm_q4_dequant(*a) == -1
+    a = list(ok); a[1] = 200
+    assert L.strata_gemm_q4_dequant(*a) == -2
+    a = list(ok); a[8] = 16
+    assert L.strata_gemm_q4_dequant(*a) == -8
+    a = list(ok); a[7] = A16 + 64
+    assert L.strata_gemm_q4_dequant(*a) == -7
