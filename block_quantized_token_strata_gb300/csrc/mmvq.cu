@@ -1160,5 +1160,4 @@ cudaError_t read_device_error_gemv(int* out, bool clear)
     return cudaMemcpyToSymbol(g_strata_device_error, &zero, sizeof(int));
 }
 
-
 }  // namespace strata
