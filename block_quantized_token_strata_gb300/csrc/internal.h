@@ -47,7 +47,7 @@ cudaError_t launch_head_argmax(const void* W, int64_t vocab, int64_t cols, int f
 cudaError_t launch_mmvq_grouped(const strata_gemv_desc* d, int n, int fmt, int T, cudaStream_t stream);
 constexpr int kMaxGroupedMatrices = 192;
 // warps per row of the GEMV for a shape (fixes the fp32 summation order; independent of T)
-int gemv_warps_per_row(int64_t cols, int fmt);
+int gemv_lanes_per_row(int64_t cols, int fmt);
 // whether the shared-memory plan of a shape fits at T
 bool gemv_shape_fits(int64_t cols, int fmt, int T);
 // device error word: bit 0 = a bounded wait in a kernel ran out (the OR of every unit's copy)

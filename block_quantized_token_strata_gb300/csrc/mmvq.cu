@@ -9,12 +9,13 @@
 // magic form, and the fp32 accumulation order and the xor tree are fixed.
 //
 // Exactness across T (column t of a T-token launch == the T = 1 launch), by construction:
-//   * a row is owned by KS warps (G = 32*KS lanes); KS is a function of (cols, fmt) only;
+//   * a row is owned by a group of G lanes: half a warp (G = 16), a warp, or KS = G/32 warps; G is
+//     a function of (cols, fmt) only;
 //   * lane g (0 <= g < G) folds blocks b = g, g+G, g+2G, ... in ascending order into
 //     acc = fma(d_w*d_x, float(isum), acc) with explicitly rounded intrinsics;
-//   * each warp combines its 32 partials in the xor order 16, 8, 4, 2, 1 (done as a butterfly
-//     reduce-scatter, which performs exactly the same pairwise additions for every value), then
-//     the KS warp sums are added in warp order;
+//   * each half-warp or warp combines its partials in the xor order (16,) 8, 4, 2, 1 (done as a
+//     butterfly reduce-scatter, which performs exactly the same pairwise additions for every value),
+//     then the KS warp sums are added in warp order;
 //   * T only sets the trip count of loops over independent columns. Nothing else depends on it.
 //
 // Data movement (GB300): a producer warp streams each CTA's contiguous rows with bulk (TMA) copies
@@ -37,8 +38,8 @@
 namespace strata {
 
 // Launch-plan tunables, fixed at compile time (the defaults are the values measured best on GB300):
-// stage size cap, ring budget, L2 prefetch distance, and the warps-per-row rule (at most KS_MAX
-// warps per row; KS doubles while every lane keeps at least KS_MINB/32 blocks).
+// stage size cap, ring budget, L2 prefetch distance, and the lanes-per-row rule (16 lanes, doubled up
+// to LPR_MAX while every lane keeps at least LPR_MINB blocks).
 #ifndef STRATA_STAGE_KB
 #define STRATA_STAGE_KB 60
 #endif
@@ -48,11 +49,14 @@ namespace strata {
 #ifndef STRATA_PF_STAGES
 #define STRATA_PF_STAGES 2
 #endif
-#ifndef STRATA_KS_MAX
-#define STRATA_KS_MAX 4
+#ifndef STRATA_LPR_MAX
+#define STRATA_LPR_MAX 128
 #endif
-#ifndef STRATA_KS_MINB
-#define STRATA_KS_MINB 64
+#ifndef STRATA_LPR_MINB
+#define STRATA_LPR_MINB 4
+#endif
+#ifndef STRATA_LPR_MINB_Q8
+#define STRATA_LPR_MINB_Q8 2
 #endif
 #ifndef STRATA_CW
 #define STRATA_CW 12
@@ -111,7 +115,7 @@ struct GemvMat {
     const float* xd;
     const int32_t* xs;
     float* y;
-    int rows, nb, ks;
+    int rows, nb, lpr;  // lpr: lanes that share a row group (16, 32, 64 or 128)
     int sg;      // chunks (row groups) per ring stage
     int chunk0;  // first chunk of this matrix in the launch's chunk sequence
 };
@@ -151,13 +155,17 @@ __device__ __forceinline__ void top2_merge(float v, int i, float s, float& bv, i
     }
 }
 
-// V values per lane -> after the five xor levels lane l holds the full sum of value vidx(l).
-template <int V>
-__device__ __forceinline__ float butterfly(float (&v)[V], int lane, int& vidx) {
+// V values per lane over a group of 2^LV lanes (LV = 5: the warp; LV = 4: a half-warp) -> after the
+// LV xor levels (2^(LV-1), ..., 2, 1) lane l holds the full group sums of values vidx(l) ..
+// vidx(l) + R - 1 in v[0 .. R-1], R = max(1, V >> LV). Every value meets the same pairwise additions
+// whatever V is: a reduce-scatter, not a different tree. `mask` names the group's lanes only: the
+// other half of a warp may have no rows in this stage and not take part.
+template <int V, int LV>
+__device__ __forceinline__ void butterfly(float (&v)[V], int lane, int& vidx, unsigned mask) {
     vidx = 0;
 #pragma unroll
-    for (int lvl = 0; lvl < 5; ++lvl) {
-        const int o = 16 >> lvl;
+    for (int lvl = 0; lvl < LV; ++lvl) {
+        const int o = (1 << (LV - 1)) >> lvl;
         const int c = (V >> lvl) > 1 ? (V >> lvl) : 1;  // values still held before this level
         if (c > 1) {
             const bool up = (lane & o) != 0;
@@ -165,14 +173,13 @@ __device__ __forceinline__ float butterfly(float (&v)[V], int lane, int& vidx) {
             for (int q = 0; q < c / 2; ++q) {
                 const float send = up ? v[q] : v[q + c / 2];
                 const float keep = up ? v[q + c / 2] : v[q];
-                v[q] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                v[q] = __fadd_rn(keep, __shfl_xor_sync(mask, send, o));
             }
             vidx += up ? c / 2 : 0;
         } else {
-            v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+            v[0] = __fadd_rn(v[0], __shfl_xor_sync(mask, v[0], o));
         }
     }
-    return v[0];
 }
 
 template <int N> struct Pow2Ceil { static constexpr int v = N <= 1 ? 1 : 2 * Pow2Ceil<(N + 1) / 2>::v; };
@@ -245,6 +252,9 @@ struct StageIter {
 };
 
 template <int FMT, int T, int MAXM, bool HEAD>
+// registers: 128 a thread. The register file is split between the SM's four schedulers (16K each) and
+// a CTA of 13 to 16 warps puts four warps on one of them, so 128 is the most either launch size
+// (13 or 16 warps) can start with.
 __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ GemvParams<MAXM> p)
 {
     constexpr int QB = FmtInfo<FMT>::kQB;
@@ -254,6 +264,10 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     constexpr int NP = (T + 1) / 2;                      // token pairs
     constexpr int RX = XRec<T, FMT>::bytes;              // activation record per block
     constexpr int kCW = cw_for(T, HEAD);                 // consumer warps of this launch
+    // sums a lane owns after a half-warp group's reduction (2 when the group's 4T values outnumber its
+    // 16 lanes), and the head's candidate slots per lane (one per owned sum)
+    constexpr int RM = V > 16 ? 2 : 1;
+    constexpr int HS = HEAD ? RM : 1;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int s_abort;
 
@@ -261,12 +275,12 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                 // full[NST], empty[NST]
     uint8_t* xsm = smem + 2 * 8 * 32;                                    // activations
     float* red = reinterpret_cast<float*>(xsm + p.nb_max * RX);          // [2][kCW][32]
-    float* hv = red + 2 * kCW * 32;                                      // head: [kCW*32] values
-    int* hi = reinterpret_cast<int*>(hv + kCW * 32);                     // head: [kCW*32] ids
-    float* hs = reinterpret_cast<float*>(hi + kCW * 32);                 // head: [kCW*32] second values
+    float* hv = red + 2 * kCW * 32;                                      // head: [HS][kCW*32] values
+    int* hi = reinterpret_cast<int*>(hv + HS * kCW * 32);                // head: [HS][kCW*32] ids
+    float* hs = reinterpret_cast<float*>(hi + HS * kCW * 32);            // head: [HS][kCW*32] second values
     // codes [NST][cstage]: an offset from `smem` (not an integer round trip), so that the compiler keeps
     // the ring in the shared address space and its reads stay shared-memory loads
-    uint8_t* cring = smem + ((reinterpret_cast<uint8_t*>(hs + kCW * 32) - smem + 127) & ~ptrdiff_t(127));
+    uint8_t* cring = smem + ((reinterpret_cast<uint8_t*>(hs + HS * kCW * 32) - smem + 127) & ~ptrdiff_t(127));
     uint8_t* sring = cring + NST * p.cstage;                                      // scales [NST][sstage]
     uint8_t* dring = sring + NST * p.sstage;                                      // Q6 d [NST][dstage]
 
@@ -397,10 +411,17 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     pdl_wait();
     pdl_launch();
 
-    float best = -FLT_MAX;
-    int bidx = INT_MAX;
-    float second = -INFINITY;  // head: the largest value this lane saw after `best` (a multiset's second)
-    int tval = 0;  // head: the token of the value this lane ends up holding
+    // head, per slot j < HS: the best value this lane saw, its row, the largest value after it (a
+    // multiset's second) and the token of the sums it holds in that slot
+    float best[HS], second[HS];
+    int bidx[HS], tval[HS];
+#pragma unroll
+    for (int j = 0; j < HS; ++j) {
+        best[j] = -FLT_MAX;
+        second[j] = -INFINITY;
+        bidx[j] = INT_MAX;
+        tval[j] = 0;
+    }
 
     SegIter<MAXM> sgi;
     sgi.init(p, g0, g1);
@@ -449,11 +470,16 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
         }
         named_bar_sync(1, kCW * 32);
 
-        const int KS = m.ks;
-        const int NG = kCW / KS;
-        const int grp = warp / KS, wig = warp - grp * KS;
-        const int G = 32 * KS;
-        const int gl = wig * 32 + lane;
+        // A row group is owned by L = m.lpr lanes: a half-warp (L = 16, two groups per warp), a warp,
+        // or KS = L / 32 warps that add their warp sums through shared memory.
+        const int L = m.lpr;
+        const bool half = L < 32;
+        const int KS = half ? 1 : L >> 5;
+        const int NG = half ? 2 * kCW : kCW / KS;
+        const int grp = half ? 2 * warp + (lane >> 4) : warp / KS;
+        const int wig = half ? 0 : warp - grp * KS;
+        const int G = L;
+        const int gl = half ? (lane & 15) : wig * 32 + lane;
         const int rsw = nb * QB;  // row stride of the codes in a stage
 
         // Every consumer warp waits on, and then releases, every stage in order — also the stages in
@@ -684,36 +710,60 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                         }
                 }
                 int vidx;
-                float tot = butterfly<V>(v, lane, vidx);
-                const bool owner = (lane & (32 / V - 1)) == 0 && vidx < kR * T;
-                const int r = vidx / T, t = vidx - (vidx / T) * T;
+                // group sums: lane l owns R consecutive values from vidx; with fewer values than
+                // lanes, each sum sits in 2^k lanes and the lowest of them owns it
+                int R = 1;
+                bool owner;
+                // this group's lanes: the whole warp, or its own half (shuffles and the warp barrier
+                // below name no lane of the other half, which may be idle in this stage)
+                const unsigned gmask = half ? (lane < 16 ? 0x0000ffffu : 0xffff0000u) : 0xffffffffu;
+                if (half) {
+                    butterfly<V, 4>(v, lane, vidx, gmask);
+                    R = V > 16 ? V / 16 : 1;
+                    owner = V >= 16 || (lane & (16 / V - 1)) == 0;
+                } else {
+                    butterfly<V, 5>(v, lane, vidx, gmask);
+                    owner = V >= 32 || (lane & (32 / V - 1)) == 0;
+                }
                 bool final_lane = (KS == 1);
-                if (KS > 1) {
+                if (KS > 1) {  // (R == 1 here: a warp holds at most 32 values)
                     float* rb = red + ((jj & 1) * kCW + warp) * 32;
-                    if (owner) rb[vidx] = tot;
+                    if (owner && vidx < kR * T) rb[vidx] = v[0];
                     named_bar_sync(2 + grp, G);
                     if (wig == 0) {
                         final_lane = true;
-                        if (owner) {
+                        if (owner && vidx < kR * T) {
                             const float* base2 = red + ((jj & 1) * kCW + grp * KS) * 32;
-                            tot = base2[vidx];
+                            float tot = base2[vidx];
                             for (int w2 = 1; w2 < KS; ++w2) tot = __fadd_rn(tot, base2[w2 * 32 + vidx]);
+                            v[0] = tot;
                         }
                     }
                 } else {
-                    __syncwarp();
+                    __syncwarp(gmask);
                 }
-                if (final_lane && owner && ok && r < nr) {
-                    const int row = row0 + r;
-                    if (m.y != nullptr) m.y[size_t(t) * rows + row] = tot;
-                    if constexpr (HEAD) {
-                        tval = t;
-                        if (better(tot, row, best, bidx)) {
-                            if (bidx != INT_MAX) second = fmaxf(second, best);
-                            best = tot;
-                            bidx = row;
-                        } else {
-                            second = fmaxf(second, tot);
+                if (final_lane && owner && ok) {
+#pragma unroll
+                    for (int j = 0; j < RM; ++j) {
+                        const int idx = vidx + j;
+                        if (j >= R || idx >= kR * T) continue;
+                        const int r = idx / T, t = idx - (idx / T) * T;
+                        if (r >= nr) continue;
+                        const float tot = v[j];
+                        const int row = row0 + r;
+                        if (m.y != nullptr) m.y[size_t(t) * rows + row] = tot;
+                        if constexpr (HEAD) {
+                            // slot j always holds the same token in this launch (vidx depends on the
+                            // lane only), so one token per slot
+                            const int js = HS > 1 ? j : 0;
+                            tval[js] = t;
+                            if (better(tot, row, best[js], bidx[js])) {
+                                if (bidx[js] != INT_MAX) second[js] = fmaxf(second[js], best[js]);
+                                best[js] = tot;
+                                bidx[js] = row;
+                            } else {
+                                second[js] = fmaxf(second[js], tot);
+                            }
                         }
                     }
                 }
@@ -730,15 +780,18 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
     }
 
     if constexpr (HEAD) {
-        hv[threadIdx.x] = best;
-        hi[threadIdx.x] = (bidx == INT_MAX) ? INT_MAX : (bidx | (tval << 27));  // token in the top bits
-        hs[threadIdx.x] = second;
+#pragma unroll
+        for (int j = 0; j < HS; ++j) {
+            hv[j * kCW * 32 + threadIdx.x] = best[j];
+            hi[j * kCW * 32 + threadIdx.x] = (bidx[j] == INT_MAX) ? INT_MAX : (bidx[j] | (tval[j] << 27));  // token in the top bits
+            hs[j * kCW * 32 + threadIdx.x] = second[j];
+        }
         named_bar_sync(1, kCW * 32);
         if (threadIdx.x < T) {
             const int t = threadIdx.x;
             float bv = -FLT_MAX, bs = -INFINITY;
             int bi = INT_MAX;
-            for (int q = 0; q < kCW * 32; ++q) {
+            for (int q = 0; q < HS * kCW * 32; ++q) {
                 const int code = hi[q];
                 if (code == INT_MAX || (code >> 27) != t) continue;
                 const int id = code & ((1 << 27) - 1);
@@ -861,16 +914,17 @@ static int qbytes_of(int fmt) { return (fmt == 0 || fmt == 3) ? 16 : (fmt == 1 ?
 // weight bytes per row group beyond the codes and the per-block 2-byte plane: Q6's super-block d
 static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : ((fmt == 3 || fmt == 4) ? (cols / 256) * 4 : 0); }
 
-// Warps per row: a function of (cols, fmt) only, so every launch of a shape (any T, single or
-// grouped) sums each row in the same order. As few warps as keep at least two blocks per lane
-// (fewer lanes per row = less reduction per block), at most four.
-int gemv_warps_per_row(int64_t cols, int fmt)
+// Lanes per row group: a function of (cols, fmt) only, so every launch of a shape (any T, single or
+// grouped) sums each row in the same order. As few lanes as keep at least LPR_MINB blocks per lane
+// (fewer lanes per row = a shorter tree per row and more blocks folded between reductions): 16
+// lanes for rows of 2,048 values, 32 for 4,096 and 6,144, 64 for 8,192.
+int gemv_lanes_per_row(int64_t cols, int fmt)
 {
-    (void)fmt;
     const int64_t nb = cols / kQK;
-    int ks = 1;
-    while (ks < STRATA_KS_MAX && nb >= int64_t(STRATA_KS_MINB) * ks * 2) ks *= 2;
-    return ks;
+    const int minb = fmt == 1 ? STRATA_LPR_MINB_Q8 : STRATA_LPR_MINB;
+    int lpr = 16;
+    while (lpr < STRATA_LPR_MAX && nb >= int64_t(minb) * lpr * 2) lpr *= 2;
+    return lpr;
 }
 
 // Chunks per ring stage: at most the group count (every group gets at most one row group of a
@@ -881,16 +935,19 @@ int gemv_warps_per_row(int64_t cols, int fmt)
 // stage size cap: the head (one long Q8 matrix) prefers smaller stages up to T = 4
 static int stage_kb(int T, bool head) { return (head && T <= 4) ? STRATA_STAGE_KB_HEAD : STRATA_STAGE_KB; }
 
-static int stage_chunks(int64_t cols, int fmt, int ks, int kCW, int stage_kb_cap)
+static int stage_chunks(int64_t cols, int fmt, int lpr, int kCW, int stage_kb_cap)
 {
     const int64_t chunk = int64_t(kR) * ((cols / kQK) * (qbytes_of(fmt) + 2) + dbytes_per_row(cols, fmt));
-    const int ng = kCW / ks;
+    const int ng = lpr < 32 ? 2 * kCW : kCW / (lpr / 32);  // row groups a CTA works on at once
     if (STRATA_SG_POW2) {
         int l = 0;
         while ((2 << l) <= ng && chunk * (2 << l) <= (int64_t(stage_kb_cap) << 10)) ++l;
         return 1 << l;
     }
     int sg = int(std::min<int64_t>(ng, (int64_t(stage_kb_cap) << 10) / chunk));
+    // half-warp groups: an even count, so that a stage's groups start on an even group and fill both
+    // halves of each warp they use (an odd start leaves one half of a warp idle for that stage)
+    if (lpr < 32 && sg >= 2) sg &= ~1;
     return std::max(sg, 1);
 }
 
@@ -922,8 +979,10 @@ static Plan plan_for(int T, const GemvMat* ms, int n, int fmt, bool head = false
     pl.sstage = int((smax + 32 + 127) & ~size_t(127));
     pl.dstage = (fmt == 2 || fmt == 3 || fmt == 4) ? int((dmax + 32 + 127) & ~size_t(127)) : 0;
     const int cw = cw_for(T, head);
+    // barriers, activation records, the cross-warp sums, the head's candidate slots (two per lane when
+    // a half-warp group holds more sums than lanes, T > 4)
     const size_t fixed = 2 * 8 * 32 + size_t(nb_max) * xrec_bytes(T, fmt) + size_t(2 * cw * 32) * 4 +
-                         size_t(cw * 32) * 12;
+                         size_t(cw * 32) * 12 * ((head && T > 4) ? 2 : 1);
     const size_t base = ((fixed + 127) & ~size_t(127)) + 128;
     const size_t per = size_t(pl.cstage) + pl.sstage + pl.dstage;
     const size_t room = base < kSmemLimit ? kSmemLimit - base : 0;
@@ -940,8 +999,8 @@ static bool shape_fits_as(int64_t cols, int fmt, int T, bool head)
 {
     GemvMat m = {};
     m.nb = int(cols / kQK);
-    m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T, head), stage_kb(T, head));
+    m.lpr = gemv_lanes_per_row(cols, fmt);
+    m.sg = stage_chunks(cols, fmt, m.lpr, cw_for(T, head), stage_kb(T, head));
     const Plan pl = plan_for(T, &m, 1, fmt, head);
     return pl.ns >= 1 && pl.smem <= kSmemLimit;
 }
@@ -978,8 +1037,8 @@ static GemvMat make_mat(const void* W, int64_t rows, int64_t cols, int fmt, cons
     m.y = y;
     m.rows = int(rows);
     m.nb = int(cols / kQK);
-    m.ks = gemv_warps_per_row(cols, fmt);
-    m.sg = stage_chunks(cols, fmt, m.ks, cw_for(T), stage_kb(T, false));
+    m.lpr = gemv_lanes_per_row(cols, fmt);
+    m.sg = stage_chunks(cols, fmt, m.lpr, cw_for(T), stage_kb(T, false));
     m.chunk0 = chunk0;
     return m;
 }
@@ -991,7 +1050,7 @@ static cudaError_t single_t(const GemvMat& m, float* cv, int* ci, cudaStream_t s
     prm.n_mat = 1;
     prm.n_chunk = (m.rows + kR - 1) / kR;
     GemvMat mm = m;
-    if (HEAD) mm.sg = stage_chunks(int64_t(m.nb) * kQK, FMT, m.ks, cw_for(T, true), stage_kb(T, true));
+    if (HEAD) mm.sg = stage_chunks(int64_t(m.nb) * kQK, FMT, m.lpr, cw_for(T, true), stage_kb(T, true));
     prm.m[0] = mm;
     prm.cand_val = cv;
     prm.cand_idx = ci;
