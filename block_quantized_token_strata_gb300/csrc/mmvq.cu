@@ -49,6 +49,9 @@ namespace strata {
 #ifndef STRATA_PF_STAGES
 #define STRATA_PF_STAGES 2
 #endif
+#ifndef STRATA_LPR_MIN
+#define STRATA_LPR_MIN 16
+#endif
 #ifndef STRATA_LPR_MAX
 #define STRATA_LPR_MAX 128
 #endif
@@ -922,7 +925,7 @@ int gemv_lanes_per_row(int64_t cols, int fmt)
 {
     const int64_t nb = cols / kQK;
     const int minb = fmt == 1 ? STRATA_LPR_MINB_Q8 : STRATA_LPR_MINB;
-    int lpr = 16;
+    int lpr = STRATA_LPR_MIN;
     while (lpr < STRATA_LPR_MAX && nb >= int64_t(minb) * lpr * 2) lpr *= 2;
     return lpr;
 }
