@@ -573,10 +573,11 @@ def bench_verify_ffn(torch, strata, synth, hbm_peak, reps=20):
     return out
 
 
-def bench_superblock_layers(torch, strata, synth, hbm_peak, fmt, layers=16, reps=20):
+def bench_superblock_layers(torch, strata, synth, hbm_peak, fmt, layers=None, reps=20):
     """The window's layer projections in a 256-weight super-block format (Q6, Q4K or Q5K; one grouped
-    launch per window; 16 layers, 0.41-0.58 GB of weights, larger than L2) at T = 2 and 4: weight
-    GB/s and HBM fraction."""
+    launch per window over the full window's 48 layers, 1.22-1.73 GB of weights) at T = 2 and 4:
+    weight GB/s and HBM fraction."""
+    layers = synth.WINDOW_LAYERS if layers is None else layers
     from block_quantized_token_strata_gb300.window import VerifyWindow, WindowWeights
     name = {synth.Q6: "Q6", synth.Q4K: "Q4K", synth.Q5K: "Q5K"}[fmt]
     wts = WindowWeights(layers=layers, device="cuda", key=f"{name}-window", layer_fmt=fmt)
