@@ -309,6 +309,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
 
     // ------------------------------------------------------------------ producer warp
     if (warp == kCW) {
+        pdl_launch();  // every thread of the CTA triggers its dependents before it waits (see below)
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             StageIter<MAXM> it, pf;
@@ -340,7 +341,6 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
             for (; it.valid(); it.next(), ++k, s = (s + 1 == NST) ? 0 : s + 1, lap += (s == 0)) {
                 if (k == NST) {  // the ring is full: from here on, order after the predecessor
                     pdl_wait();
-                    pdl_launch();
                     waited = true;
                 }
                 if (k >= NST) {
@@ -391,10 +391,7 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 if (mid) bulk_g2s(smem_u32(sdst + head), ssrc + head, mid, fb, pol);
                 if (dmid) bulk_g2s(smem_u32(ddst + dhead), dsrc + dhead, dmid, fb, pol);
             }
-            if (!waited) {
-                pdl_wait();
-                pdl_launch();
-            }
+            if (!waited) pdl_wait();
             // no copy may still be landing in shared memory when the CTA leaves: the issued copies are
             // waited for (bounded) even after an abort
             const int no_abort = 0;
@@ -405,14 +402,15 @@ __global__ void __maxnreg__(STRATA_MAXNREG) gemv_kernel(const __grid_constant__ 
                 }
         } else {
             pdl_wait();
-            pdl_launch();
         }
         return;
     }
 
     // ------------------------------------------------------------------ consumer warps
-    pdl_wait();
+    // Dependents may launch now (they wait for this grid's completion before they read what it
+    // writes, and can stream their weights meanwhile); this grid's own inputs come after the wait.
     pdl_launch();
+    pdl_wait();
 
     // head, per slot j < HS: the best value this lane saw, its row, the largest value after it (a
     // multiset's second) and the token of the sums it holds in that slot
@@ -816,8 +814,8 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const float* __restr
                                                             int T, int32_t* __restrict__ ids,
                                                             float* __restrict__ margin)
 {
-    pdl_wait();
     pdl_launch();
+    pdl_wait();
     const int t = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -849,8 +847,8 @@ __global__ void __launch_bounds__(256) block_dots_kernel(const uint8_t* __restri
                                                          const int32_t* __restrict__ xs, int T,
                                                          int32_t* __restrict__ isum)
 {
-    pdl_wait();
     pdl_launch();
+    pdl_wait();
     constexpr int QB = FmtInfo<FMT>::kQB;
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= int64_t(rows) * nb) return;
@@ -1054,10 +1052,10 @@ static cudaError_t single_t(const GemvMat& m, float* cv, int* ci, cudaStream_t s
     prm.n_chunk = (m.rows + kR - 1) / kR;
     GemvMat mm = m;
     if (HEAD) mm.sg = stage_chunks(int64_t(m.nb) * kQK, FMT, m.lpr, cw_for(T, true), stage_kb(T, true));
+    const int grid = std::min(prm.n_chunk, kCtasPerSm * device_sm_count());
     prm.m[0] = mm;
     prm.cand_val = cv;
     prm.cand_idx = ci;
-    const int grid = std::min(prm.n_chunk, kCtasPerSm * device_sm_count());
     prm.cand_sec = (HEAD && ci) ? reinterpret_cast<float*>(ci + size_t(grid) * T) : nullptr;  // [T][grid] after ids
     if (grid_out) *grid_out = grid;
     if (HEAD && cv == nullptr) return cudaSuccess;  // size query

@@ -17,8 +17,8 @@ __global__ void __launch_bounds__(256)
 quantize_act_kernel(const float4* __restrict__ x, int64_t nblk, int* __restrict__ xq,
                     float* __restrict__ xd, int32_t* __restrict__ xs)
 {
+    pdl_launch();   // the next kernel may launch and stream its weights meanwhile
     pdl_wait();     // x may be the output of the kernel ahead of this one
-    pdl_launch();
     const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t blk = gid >> 3;
     const int sub = threadIdx.x & 7;

@@ -21,11 +21,14 @@
  *   - Every call validates its arguments on the host first and returns a status code without
  *     launching anything when they are wrong. Otherwise it enqueues kernels on `stream` and
  *     returns at once (asynchronous); STRATA_ERR_CUDA reports a launch failure.
- *   - Kernels are launched with programmatic dependent launch. Activations, outputs and workspace
- *     are touched only after the preceding kernel on the stream has completed; WEIGHTS may be read
- *     (prefetched into L2) while the preceding kernel is still running, so weight buffers must be
- *     fully written before the kernel launched just ahead of the call on the same stream begins
- *     (weights are static model data; a cudaMemcpy on the stream is a full dependency and is fine).
+ *   - Kernels are launched with programmatic dependent launch, and every kernel lets the next one
+ *     launch before it waits for its own predecessor. Activations, outputs and workspace are
+ *     touched only after the preceding kernel on the stream has completed; WEIGHTS may be read
+ *     (streamed, prefetched into L2) while earlier kernels of this library on the stream are still
+ *     running, back to the nearest operation on the stream that is not a kernel of this library (a
+ *     copy, an event wait, another kernel), which completes before anything after it starts. So
+ *     weight buffers must be fully written before that operation completes (weights are static
+ *     model data; a cudaMemcpy on the stream is a full dependency and is fine).
  *   - Floating point is IEEE fp32 with round-to-nearest; no fast-math.
  *
  * Block formats (32 weights per block along a row; cols % 32 == 0; nb = cols / 32).
