@@ -110,13 +110,15 @@ class VerifyWindow:
             return 1 + 1 + 2                    # one quantize, grouped GEMV, head + finalize
         return 2 * (len(self.shapes) - 1) + 3   # quantize + GEMV per layer matrix; quantize + head + finalize
 
-    def enqueue(self, stream=None, part: str = "all") -> None:
-        """Enqueue one window (``part``: "all", "layers" = everything before the head, "head")."""
+    def enqueue(self, stream=None, part: str = "all", x_src: torch.Tensor | None = None) -> None:
+        """Enqueue one window (``part``: "all", "layers" = everything before the head, "head"). In the
+        grouped mode ``x_src`` (a buffer shaped like ``x_flat``) replaces ``x_flat`` as the input."""
         n = len(self.shapes)
         name, vocab, hcols, hfmt = self.shapes[-1]
         if self.mode == "grouped":
             if part in ("all", "layers"):
-                strata.quantize_act(self.x_flat.view(1, -1), self.q_flat.view(1, -1), self.d_flat.view(1, -1),
+                xs = self.x_flat if x_src is None else x_src
+                strata.quantize_act(xs.view(1, -1), self.q_flat.view(1, -1), self.d_flat.view(1, -1),
                                     self.s_flat.view(1, -1), stream=stream)
                 strata.mmvq_grouped(self.descs, self.wts.layer_fmt, self.T, stream=stream)
         else:
@@ -132,16 +134,16 @@ class VerifyWindow:
             strata.head_argmax(self.wts.dev[n - 1], vocab, hcols, hfmt, self.xq[n - 1], self.xd[n - 1],
                                self.xs[n - 1], self.T, self.ids, self.y[n - 1], self.head_ws, stream=stream)
 
-    def capture(self, part: str = "all") -> torch.cuda.CUDAGraph:
+    def capture(self, part: str = "all", x_src: torch.Tensor | None = None) -> torch.cuda.CUDAGraph:
         """One CUDA graph of ``part`` of the step, after one eager warm-up pass on a side stream."""
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.enqueue(part=part)
+            self.enqueue(part=part, x_src=x_src)
         torch.cuda.current_stream().wait_stream(s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.enqueue(part=part)
+            self.enqueue(part=part, x_src=x_src)
         return g
 
     def run_host(self, graph: torch.cuda.CUDAGraph, x_host: torch.Tensor, ids_host: torch.Tensor) -> None:
@@ -150,3 +152,42 @@ class VerifyWindow:
         self.x_flat.copy_(x_host, non_blocking=True)
         graph.replay()
         ids_host.copy_(self.ids, non_blocking=True)
+
+
+class HostPipeline:
+    """Windows fed from host memory, each step's input copy overlapped with the previous window's
+    compute: two device input buffers, a CUDA graph of the whole (grouped) window for each, and a copy
+    stream. Every step still copies its own fp32 inputs host -> device and its ids device -> host; the
+    copy into a buffer waits only for the window that last read that buffer."""
+
+    def __init__(self, win: VerifyWindow):
+        assert win.mode == "grouped"
+        self.win = win
+        self.xbuf = [win.x_flat, torch.empty_like(win.x_flat)]
+        self.graphs = [win.capture(), win.capture(x_src=self.xbuf[1])]
+        self.copy_stream = torch.cuda.Stream()
+        self.copied = [torch.cuda.Event(), torch.cuda.Event()]
+        self.consumed = [torch.cuda.Event(), torch.cuda.Event()]  # the window that read buffer j is done
+
+    def _copy(self, j: int, x_host: torch.Tensor) -> None:
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.consumed[j])
+            self.xbuf[j].copy_(x_host, non_blocking=True)
+            self.copied[j].record(self.copy_stream)
+
+    def run(self, x_hosts, ids_hosts) -> None:
+        """Windows k = 0 .. len(x_hosts) - 1 on the current stream (asynchronous): window k reads
+        x_hosts[k] (pinned fp32, laid out as ``x_flat``) and leaves its ids in ids_hosts[k] (pinned)."""
+        cur = torch.cuda.current_stream()
+        self.copy_stream.wait_stream(cur)  # nothing of this run starts before the work already enqueued
+        n = len(x_hosts)
+        if n:
+            self._copy(0, x_hosts[0])
+        for k in range(n):
+            j = k & 1
+            if k + 1 < n:
+                self._copy(j ^ 1, x_hosts[k + 1])   # streams in while window k computes
+            cur.wait_event(self.copied[j])
+            self.graphs[j].replay()
+            self.consumed[j].record(cur)
+            ids_hosts[k].copy_(self.win.ids, non_blocking=True)

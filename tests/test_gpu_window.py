@@ -129,3 +129,28 @@ def test_full_window_replays_clean_at_high_T(weights, T):
     for a, b in zip(wg.y, wc.y):
         assert torch.equal(_bits(a), _bits(b))
     assert torch.equal(wg.ids, wc.ids)
+
+
+def test_host_pipeline_matches_plain_runs(weights):
+    """The end-to-end loop: each step's host input copy overlaps the previous window (two device
+    input buffers, a graph each, a copy stream). Two input sets alternate over six steps; every
+    step's ids equal those of a plain run on the same inputs."""
+    from block_quantized_token_strata_gb300.window import HostPipeline
+    w = VerifyWindow(weights, 4, mode="grouped")
+    host = [w.host_inputs()]
+    host.append(np.ascontiguousarray(host[0][::-1]))
+    want = []
+    for h in host:
+        w.load_inputs(h)
+        w.enqueue()
+        torch.cuda.synchronize()
+        want.append(w.ids.cpu().numpy().copy())
+    pipe = HostPipeline(w)
+    x_hosts = [torch.from_numpy(h).pin_memory() for h in host]
+    ids_hosts = [torch.empty(4, dtype=torch.int32).pin_memory() for _ in range(6)]
+    strata.device_error(clear=True)
+    pipe.run([x_hosts[k & 1] for k in range(6)], ids_hosts)
+    torch.cuda.synchronize()
+    assert strata.device_error(clear=True) == 0
+    for k in range(6):
+        assert np.array_equal(ids_hosts[k].numpy(), want[k & 1]), k
