@@ -83,6 +83,7 @@ SHAPES = [
     (synth.Q4, 33, 96, 3, False),        # ragged: rows not a multiple of any row group, 3 blocks
     (synth.Q8, 1, 32, 8, False),         # one row, one block
     (synth.Q4, 1000, 2080, 5, True),     # 65 blocks: lane 0 takes three blocks, others two
+    (synth.Q4, 512, 2048, 4, False),     # one row group per CTA: one half-warp group of a warp has rows, the other none
     (synth.Q4, 5120, 2048, 4, False),    # window qkv
     (synth.Q4, 2048, 6144, 4, False),    # window down
 ]
