@@ -38,8 +38,8 @@
 namespace strata {
 
 // Launch-plan tunables, fixed at compile time (the defaults are the values measured best on GB300):
-// stage size cap, ring budget, L2 prefetch distance, and the lanes-per-row rule (16 lanes, doubled up
-// to LPR_MAX while every lane keeps at least LPR_MINB blocks).
+// stage size cap, ring budget, L2 prefetch distance, and the lanes-per-row rule (LPR_MIN lanes,
+// doubled up to LPR_MAX while every lane keeps at least the format's kMinBlocksPerLane blocks).
 #ifndef STRATA_STAGE_KB
 #define STRATA_STAGE_KB 60
 #endif
@@ -54,12 +54,6 @@ namespace strata {
 #endif
 #ifndef STRATA_LPR_MAX
 #define STRATA_LPR_MAX 128
-#endif
-#ifndef STRATA_LPR_MINB
-#define STRATA_LPR_MINB 4
-#endif
-#ifndef STRATA_LPR_MINB_Q8
-#define STRATA_LPR_MINB_Q8 2
 #endif
 #ifndef STRATA_CW
 #define STRATA_CW 12
@@ -916,13 +910,18 @@ static int qbytes_of(int fmt) { return (fmt == 0 || fmt == 3) ? 16 : (fmt == 1 ?
 static int64_t dbytes_per_row(int64_t cols, int fmt) { return fmt == 2 ? (cols / 256) * 2 : ((fmt == 3 || fmt == 4) ? (cols / 256) * 4 : 0); }
 
 // Lanes per row group: a function of (cols, fmt) only, so every launch of a shape (any T, single or
-// grouped) sums each row in the same order. As few lanes as keep at least LPR_MINB blocks per lane
-// (fewer lanes per row = a shorter tree per row and more blocks folded between reductions): 16
-// lanes for rows of 2,048 values, 32 for 4,096 and 6,144, 64 for 8,192.
+// grouped) sums each row in the same order. As few lanes as keep at least the format's
+// kMinBlocksPerLane blocks per lane (fewer lanes per row = a shorter tree per row and more blocks
+// folded between reductions): for Q4, 16 lanes for rows of 2,048 values, 32 for 4,096 and 6,144, 64
+// for 8,192.
+// The blocks each lane keeps at least, per format (Q4, Q8, Q6, Q4K, Q5K): the GB300 sweep's winners
+// over 2, 3 and 4 on the verify window's 48 layers at T = 2 and 4 (Q8: the vocabulary head).
+constexpr int kMinBlocksPerLane[5] = {4, 2, 2, 4, 3};
+
 int gemv_lanes_per_row(int64_t cols, int fmt)
 {
     const int64_t nb = cols / kQK;
-    const int minb = fmt == 1 ? STRATA_LPR_MINB_Q8 : STRATA_LPR_MINB;
+    const int minb = kMinBlocksPerLane[(fmt >= 0 && fmt < 5) ? fmt : 0];
     int lpr = STRATA_LPR_MIN;
     while (lpr < STRATA_LPR_MAX && nb >= int64_t(minb) * lpr * 2) lpr *= 2;
     return lpr;
