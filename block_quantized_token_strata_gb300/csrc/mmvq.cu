@@ -932,8 +932,17 @@ int gemv_lanes_per_row(int64_t cols, int fmt)
 #ifndef STRATA_STAGE_KB_HEAD
 #define STRATA_STAGE_KB_HEAD 36
 #endif
-// stage size cap: the head (one long Q8 matrix) prefers smaller stages up to T = 4
-static int stage_kb(int T, bool head) { return (head && T <= 4) ? STRATA_STAGE_KB_HEAD : STRATA_STAGE_KB; }
+#ifndef STRATA_STAGE_KB_HI_T
+#define STRATA_STAGE_KB_HI_T 48
+#endif
+// stage size cap (it only schedules work): the head (one long Q8 matrix) prefers smaller stages up
+// to T = 4; from T = 5 the wider activation records leave less room, and 48 KB stages beat 60 KB
+// (the T = 8 window: 541 -> 512 us)
+static int stage_kb(int T, bool head)
+{
+    if (head) return T <= 4 ? STRATA_STAGE_KB_HEAD : STRATA_STAGE_KB;
+    return T >= 5 ? STRATA_STAGE_KB_HI_T : STRATA_STAGE_KB;
+}
 
 static int stage_chunks(int64_t cols, int fmt, int lpr, int kCW, int stage_kb_cap)
 {
